@@ -1,0 +1,355 @@
+"""fp64 oracle of one sampler step (test infrastructure; see the package
+docstring).
+
+Every row r of the batch carries a phase and is processed by it, as in the
+vLLM blog's single vectorised sample step (section "Putting it together:
+DiffusionGemmaModelState and DiffusionSampler"):
+
+* PREFILL -- the canvas becomes uniform random tokens; nothing is sampled.
+* DENOISE -- per position i: tempered logits y = z / T, softmax p, entropy
+  H = -sum p ln p ("DiffusionGemma Explained", "Sampling", step 2), clean
+  argmax of z, Gumbel-max candidate argmax(y + G) (vLLM blog, sampler
+  bullet "denoising").  Then entropy-bounded acceptance: positions sorted by
+  (H, i) ascending are accepted while the exclusive prefix sum of entropies
+  stays within the budget ("DiffusionGemma Explained", "Sampling", step 3;
+  Technical Report section 3.3 "Entropy-bounded token refinement"); the first
+  is always accepted.  Rejected positions are re-noised to uniform tokens
+  (Technical Report section 3.3).  Convergence: the argmax canvas equal to
+  the previous step's for ``stable_k`` consecutive steps and mean entropy
+  below the threshold, or the step cap (vLLM blog, same section; Technical
+  Report section 3.3 "Adaptive stopping heuristic").
+* COMMIT  -- emit the clean argmax canvas of the last denoise step, re-draw
+  the canvas for the next block and reset the per-request counters (vLLM
+  blog, sampler bullet "commit").
+* IDLE    -- untouched.
+
+Readings where the pages are silent or disagree are listed in the design doc's
+readings table; the ones that change results are restated next to the code.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import rng
+
+PHASE_PREFILL = 0
+PHASE_DENOISE = 1
+PHASE_COMMIT = 2
+PHASE_IDLE = 3
+
+NEAR_TIE = 1e-4  # gap below which an index decision is flagged, not compared
+
+
+@dataclass
+class Params:
+    batch: int
+    canvas_len: int
+    vocab: int
+    seed: int
+    entropy_budget: float
+    conf_threshold: float
+    stable_k: int
+    step_cap: int
+
+
+@dataclass
+class State:
+    """Per-request state; arrays are numpy, shapes [B] or [B, C]."""
+
+    phase: np.ndarray          # uint8 [B]
+    request_id: np.ndarray     # uint64 [B]
+    temperature: np.ndarray    # float [B]
+    rng_step: np.ndarray       # uint64 [B]
+    step: np.ndarray           # int32 [B]
+    stable: np.ndarray         # int32 [B]
+    canvas: np.ndarray         # int32 [B, C]
+    argmax_prev: np.ndarray    # int32 [B, C]
+    cand: np.ndarray = None    # int32 [B, C]
+    argmax: np.ndarray = None  # int32 [B, C]
+    accept: np.ndarray = None  # uint8 [B, C]
+    m: np.ndarray = None       # float64 [B, C]
+    s: np.ndarray = None       # float64 [B, C]
+    entropy: np.ndarray = None  # float64 [B, C]
+    mean_entropy: np.ndarray = None  # float64 [B]
+    converged: np.ndarray = None     # uint8 [B]
+    sc_valid: np.ndarray = None      # uint8 [B]
+    num_sampled: np.ndarray = None   # int32 [B]
+    num_rejected: np.ndarray = None  # int32 [B]
+    emitted: np.ndarray = None       # int32 [B, C]
+
+    def copy(self):
+        out = State(**{k: (None if v is None else np.array(v, copy=True))
+                       for k, v in self.__dict__.items()})
+        return out
+
+
+@dataclass
+class Flags:
+    """Near-tie flags: where fp64 and any fp32 evaluation may legitimately
+    take a different discrete decision (gap or distance below 1e-4)."""
+
+    cand: np.ndarray = None      # bool [B, C]: top-2 perturbed-score gap < 1e-4
+    accept: np.ndarray = None    # bool [B]: acceptance cut within 1e-4
+    converged: np.ndarray = None  # bool [B]: |mean H - thr| < 1e-4
+    gaps: np.ndarray = None      # float64 [B, C]
+
+
+# --------------------------------------------------------------------------
+# per position
+
+
+@dataclass
+class PositionResult:
+    valid: bool
+    m: float
+    s: float
+    entropy: float
+    argmax: int
+    cand: int
+    gap: float
+
+
+def gumbel_keys(seed, request_id, rng_step, position):
+    p = rng.position_key(seed, request_id, rng_step, position)
+    return (rng.stream_key(p, rng.TAG_GMIN), rng.stream_key(p, rng.TAG_GARG),
+            rng.stream_key(p, rng.TAG_GREST))
+
+
+def vocab_pass(z, T, ka, kb, kc) -> PositionResult:
+    """All per-position quantities of one logit row ``z`` (float64, the stored
+    logits widened exactly) at temperature ``T``.
+
+    Validity (a reading; the pages are silent): a row holding a NaN or a +inf
+    logit, a row whose logits are all -inf, or a non-positive / non-finite
+    temperature is invalid: entropy, m and s are NaN, argmax = cand = 0.
+    -inf logits in a valid row are tokens of probability zero.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    V = z.size
+    bad = (not (T > 0.0 and math.isfinite(T)) or np.isnan(z).any()
+           or np.isposinf(z).any() or not np.isfinite(z).any())
+    if bad:
+        return PositionResult(False, math.nan, math.nan, math.nan, 0, 0, math.inf)
+    # temperature (Technical Report eq. 6: Softmax(L_t / tau_t))
+    y = z / T
+    # softmax with max subtraction: p_v = exp(y_v - m) / s
+    m = float(np.max(y))
+    e = np.exp(y - m)
+    s = float(np.sum(e))
+    p = e / s
+    # entropy -sum p ln p over the support ("DiffusionGemma Explained", step 2)
+    nz = p > 0
+    H = float(-np.sum(p[nz] * np.log(p[nz])))
+    # clean argmax, lowest index on ties (vLLM blog: the argmax canvas)
+    am = int(np.argmax(z))
+    # Gumbel-max candidate argmax(y + G), lowest index on ties
+    G = rng.gumbel_noise(V, ka, kb, kc)
+    score = y + G
+    cand = int(np.argmax(score))
+    if V > 1:
+        rest = np.delete(score, cand)
+        gap = float(score[cand] - np.max(rest))
+    else:
+        gap = math.inf
+    return PositionResult(True, m, s, H, am, cand, gap)
+
+
+# --------------------------------------------------------------------------
+# per canvas
+
+
+def accept_mask(H, budget):
+    """Entropy-bounded acceptance of one canvas.
+
+    Positions sorted by (H_i, i) ascending (invalid positions, H = NaN, sort
+    last as +inf); the k-th in that order is accepted iff k = 0 or the sum of
+    the entropies before it is <= budget ("DiffusionGemma Explained",
+    "Sampling", step 3: the largest prefix whose exclusive sum stays within
+    the bound).  Invalid positions (a reading; the pages are silent) are
+    never accepted, so a canvas with no valid position accepts nothing.
+    Returns (accept[C] bool, flagged) where ``flagged`` says that the cut
+    lies within 1e-4 of a decision boundary.
+    """
+    H = np.asarray(H, dtype=np.float64)
+    C = H.size
+    key = np.where(np.isnan(H), np.inf, H)
+    order = sorted(range(C), key=lambda i: (key[i], i))
+    acc = np.zeros(C, dtype=bool)
+    prefix = 0.0
+    flagged = False
+    for k, i in enumerate(order):
+        if k > 0 and abs(prefix - budget) < NEAR_TIE:
+            flagged = True
+        if np.isfinite(key[i]) and (k == 0 or prefix <= budget):
+            acc[i] = True
+        prefix = prefix + key[i]
+    n_acc = int(acc.sum())
+    if 0 < n_acc < C:
+        a, b = key[order[n_acc - 1]], key[order[n_acc]]
+        if abs(b - a) < NEAR_TIE:
+            flagged = True
+    return acc, flagged
+
+
+def renoise_tokens(seed, request_id, rng_step, C, V):
+    p = rng.position_key(seed, request_id, rng_step, np.arange(C, dtype=np.uint64))
+    return rng.uniform_token(rng.stream_key(p, rng.TAG_RENOISE), V).astype(np.int32)
+
+
+def init_tokens(seed, request_id, rng_step, C, V):
+    p = rng.position_key(seed, request_id, rng_step, np.arange(C, dtype=np.uint64))
+    return rng.uniform_token(rng.stream_key(p, rng.TAG_INIT), V).astype(np.int32)
+
+
+def _ensure_outputs(st: State, B, C):
+    def z(shape, dt, fill=0):
+        return np.full(shape, fill, dtype=dt)
+    if st.cand is None: st.cand = z((B, C), np.int32)
+    if st.argmax is None: st.argmax = z((B, C), np.int32)
+    if st.accept is None: st.accept = z((B, C), np.uint8)
+    if st.m is None: st.m = z((B, C), np.float64, np.nan)
+    if st.s is None: st.s = z((B, C), np.float64, np.nan)
+    if st.entropy is None: st.entropy = z((B, C), np.float64, np.nan)
+    if st.mean_entropy is None: st.mean_entropy = z((B,), np.float64, np.nan)
+    if st.converged is None: st.converged = z((B,), np.uint8)
+    if st.sc_valid is None: st.sc_valid = z((B,), np.uint8)
+    if st.num_sampled is None: st.num_sampled = z((B,), np.int32)
+    if st.num_rejected is None: st.num_rejected = z((B,), np.int32)
+    if st.emitted is None: st.emitted = z((B, C), np.int32)
+
+
+def prefill_row(p: Params, st: State, r: int):
+    """Canvas of uniform random tokens (Technical Report section 3.2 "Canvas
+    initialization"; vLLM blog: prefill initialises the canvas and samples
+    nothing).  num_rejected = 0 is a reading (the blog names only
+    num_sampled)."""
+    C, V = p.canvas_len, p.vocab
+    st.canvas[r] = init_tokens(p.seed, st.request_id[r], st.rng_step[r], C, V)
+    st.step[r] = 0
+    st.stable[r] = 0
+    st.num_sampled[r] = 0
+    st.num_rejected[r] = 0
+    st.sc_valid[r] = 0
+    st.converged[r] = 0
+    st.phase[r] = PHASE_DENOISE
+    st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+
+
+def commit_row(p: Params, st: State, r: int):
+    """Emit the clean argmax canvas of the last denoise step (vLLM blog: the
+    committed tokens are the clean argmax prediction), then start the next
+    block from a fresh random canvas with reset counters."""
+    C, V = p.canvas_len, p.vocab
+    st.emitted[r] = st.argmax_prev[r]
+    st.num_sampled[r] = C
+    st.num_rejected[r] = 0
+    st.canvas[r] = init_tokens(p.seed, st.request_id[r], st.rng_step[r], C, V)
+    st.step[r] = 0
+    st.stable[r] = 0
+    st.sc_valid[r] = 0
+    st.converged[r] = 0
+    st.phase[r] = PHASE_DENOISE
+    st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+
+
+def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags):
+    """One denoise step of row r from its logits ``logits_row`` [C, V]."""
+    C, V = p.canvas_len, p.vocab
+    T = float(st.temperature[r])
+    H = np.empty(C)
+    for i in range(C):
+        ka, kb, kc = gumbel_keys(p.seed, st.request_id[r], st.rng_step[r], i)
+        res = vocab_pass(logits_row[i], T, ka, kb, kc)
+        st.m[r, i] = res.m
+        st.s[r, i] = res.s
+        st.entropy[r, i] = res.entropy
+        st.argmax[r, i] = res.argmax
+        st.cand[r, i] = res.cand
+        flags.gaps[r, i] = res.gap
+        flags.cand[r, i] = res.gap < NEAR_TIE
+        H[i] = res.entropy
+    acc, aflag = accept_mask(H, p.entropy_budget)
+    flags.accept[r] = aflag
+    st.accept[r] = acc.astype(np.uint8)
+    R = renoise_tokens(p.seed, st.request_id[r], st.rng_step[r], C, V)
+    st.canvas[r] = np.where(acc, st.cand[r], R)
+    # convergence (vLLM blog; Technical Report "Adaptive stopping heuristic")
+    same = bool(st.step[r] > 0 and np.all(st.argmax[r] == st.argmax_prev[r]))
+    st.stable[r] = st.stable[r] + 1 if same else 0
+    Hbar = float(np.sum(H) / C)
+    st.mean_entropy[r] = Hbar
+    st.step[r] = st.step[r] + 1
+    st.argmax_prev[r] = st.argmax[r]
+    conv = (st.stable[r] >= p.stable_k and Hbar < p.conf_threshold) or st.step[r] >= p.step_cap
+    flags.converged[r] = (not math.isnan(Hbar)) and abs(Hbar - p.conf_threshold) < NEAR_TIE
+    st.converged[r] = 1 if conv else 0
+    st.sc_valid[r] = 0 if conv else 1
+    st.phase[r] = PHASE_COMMIT if conv else PHASE_DENOISE
+    st.num_sampled[r] = 0
+    st.num_rejected[r] = C
+    st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+
+
+def step(p: Params, st_in: State, logits, rows=None):
+    """One sampler call over the whole batch: each row by its phase.
+
+    ``logits`` is indexable as logits[r] -> [C, V] float64 (or convertible);
+    rows other than DENOISE rows are not read.  ``rows`` optionally limits
+    which DENOISE rows are evaluated (the others are left untouched, which is
+    how large configurations are checked on a sample).  Returns the new
+    state and the near-tie flags; ``st_in`` is not modified.
+    """
+    B, C = p.batch, p.canvas_len
+    st = st_in.copy()
+    _ensure_outputs(st, B, C)
+    flags = Flags(cand=np.zeros((B, C), bool), accept=np.zeros(B, bool),
+                  converged=np.zeros(B, bool), gaps=np.full((B, C), np.inf))
+    for r in range(B):
+        ph = int(st.phase[r])
+        if ph == PHASE_PREFILL:
+            prefill_row(p, st, r)
+        elif ph == PHASE_COMMIT:
+            commit_row(p, st, r)
+        elif ph == PHASE_DENOISE:
+            if rows is not None and r not in rows:
+                continue
+            denoise_row(p, st, r, np.asarray(logits[r], dtype=np.float64), flags)
+    return st, flags
+
+
+def init_rows(p: Params, st_in: State, row_mask):
+    """Stand-alone canvas initialisation of the masked rows (prefill form)."""
+    st = st_in.copy()
+    _ensure_outputs(st, p.batch, p.canvas_len)
+    for r in range(p.batch):
+        if row_mask[r]:
+            prefill_row(p, st, r)
+    return st
+
+
+def commit_rows(p: Params, st_in: State, row_mask):
+    """Stand-alone commit of the masked rows."""
+    st = st_in.copy()
+    _ensure_outputs(st, p.batch, p.canvas_len)
+    for r in range(p.batch):
+        if row_mask[r]:
+            commit_row(p, st, r)
+    return st
+
+
+def new_state(p: Params, phase, request_id, temperature, rng_step=None):
+    B, C = p.batch, p.canvas_len
+    st = State(
+        phase=np.asarray(phase, dtype=np.uint8).copy(),
+        request_id=np.asarray(request_id, dtype=np.uint64).copy(),
+        temperature=np.asarray(temperature, dtype=np.float64).copy(),
+        rng_step=(np.zeros(B, np.uint64) if rng_step is None
+                  else np.asarray(rng_step, dtype=np.uint64).copy()),
+        step=np.zeros(B, np.int32), stable=np.zeros(B, np.int32),
+        canvas=np.zeros((B, C), np.int32), argmax_prev=np.zeros((B, C), np.int32))
+    _ensure_outputs(st, B, C)
+    return st
