@@ -1,0 +1,449 @@
+#!/usr/bin/env python3
+"""Benchmark of the denoise-step hot path: one step = dg_denoise_step (fused
+vocabulary pass + per-canvas acceptance / re-noise / convergence) followed by
+dg_selfcond_embed (the tcgen05 softmax(z/T).E contraction), over one batch of
+synthetic logits resident in HBM.
+
+Default workload: 8 canvases x 256 positions (2048 positions), V = 262144,
+bf16 logits N(0, 2^2) plus U[0,16) on one token per position, T = 0.8,
+budget 96 nats, E 262144 x 2816 bf16 ~ N(0, 0.02^2).  The step cap is lifted
+so that every timed step does the full work (all rows stay in DENOISE and
+feed the self-conditioning).  Inputs (1.07 GB logits, 1.48 GB E) are larger
+than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
+on the same workload instead (a bounded sample per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (B, C, V, dtype, T, budget, d, boost_hi)
+    "8x256-V262144-bf16-d2816": (8, 256, 262144, "bf16", 0.8, 96.0, 2816, 16.0),
+    "1x256-V50257-f32-d512": (1, 256, 50257, "f32", 1.0, 64.0, 512, 12.0),
+    "16x256-V262144-bf16-d2816": (16, 256, 262144, "bf16", 0.8, 128.0, 2816, 16.0),
+    "32x256-V262144-bf16-d2816": (32, 256, 262144, "bf16", 0.8, 128.0, 2816, 16.0),
+    "64x256-V262144-bf16-d2816": (64, 256, 262144, "bf16", 0.8, 128.0, 2816, 16.0),
+    "128x256-V262144-bf16-d2816": (128, 256, 262144, "bf16", 0.8, 128.0, 2816, 16.0),
+    "1x256-V262144-bf16-d2816": (1, 256, 262144, "bf16", 0.8, 96.0, 2816, 16.0),
+}
+DEFAULT = "8x256-V262144-bf16-d2816"
+METRIC = "denoise-step positions/s (sampler+self-cond)"
+SEED = 0xD1FF0002
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_id_for(dev) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev] if vis else str(dev)
+
+
+# ---------------------------------------------------------- CPU oracle leg
+
+def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None = None):
+    """Time the fp64 oracle on a bounded sample of the workload: P positions of
+    canvas 0 (vocabulary pass each, canvas-level acceptance on their
+    entropies) plus their self-conditioning rows through one fp64 matmul.
+    Returns (positions/s, P, seconds)."""
+    import torch
+    from denoise_step_sampler_gb300 import synthetic as syn
+    from oracle import sampler as osam
+    from oracle import selfcond as osc
+
+    B, C, V, dt, T, budget, d, boost = WORKLOADS[wl_name]
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    # probe one position to size the sample
+    P = 1
+    z = syn.boosted_logits(P, V, seed=SEED, dtype=tdt, device="cpu", boost_hi=boost).float().numpy()
+    E = syn.embedding(V, d, seed=SEED, device="cpu").float().numpy().astype(np.float64)
+    Tf = float(np.float32(T))
+
+    def run(zrows):
+        t0 = time.perf_counter()
+        H = []
+        for i in range(zrows.shape[0]):
+            ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
+            H.append(osam.vocab_pass(zrows[i].astype(np.float64), Tf, ka, kb, kc).entropy)
+        osam.accept_mask(np.resize(np.asarray(H), C), budget)
+        osc.selfcond_rows(zrows.astype(np.float64), Tf, E)
+        return time.perf_counter() - t0
+
+    t1 = run(z)
+    P = max(1, int(budget_s / max(t1, 1e-3)))
+    if max_positions:
+        P = min(P, max_positions)
+    z = syn.boosted_logits(P, V, seed=SEED, dtype=tdt, device="cpu", boost_hi=boost).float().numpy()
+    t = run(z)
+    return P / t, P, t
+
+
+def cpu_baseline_subprocess(wl_name: str, budget_s: float = 12.0):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-oracle-leg", "--workload", wl_name,
+           "--cpu-budget", str(budget_s)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
+    for line in r.stdout.splitlines()[::-1]:
+        if line.startswith("{"):
+            return json.loads(line)
+    raise RuntimeError("cpu oracle leg failed: " + r.stderr[-2000:])
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, dev):
+    import torch
+    import torch.distributed as dist
+    import denoise_step_sampler_gb300 as dg
+    from denoise_step_sampler_gb300 import build as dgbuild
+    from denoise_step_sampler_gb300 import synthetic as syn
+
+    if rank == 0:
+        dgbuild.build()
+    if world > 1:
+        dist.barrier()
+    dg.lib()
+
+    B, C, V, dt, T, budget, d, boost = WORKLOADS[args.workload]
+    if args.batch:
+        B = args.batch
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    esz = 2 if dt == "bf16" else 4
+    p = dg.Params(batch=B, canvas_len=C, vocab=V,
+                  logits_dtype=dg.DG_BF16 if dt == "bf16" else dg.DG_F32,
+                  seed=SEED, entropy_budget=budget, conf_threshold=0.3, stable_k=3,
+                  step_cap=1 << 30)
+    logits = syn.boosted_logits(B * C, V, seed=SEED + rank, dtype=tdt, device=dev,
+                                boost_hi=boost).reshape(-1)
+    E = syn.embedding(V, d, seed=SEED, device=dev)
+    st = dg.State(B, C, dev)
+    st.phase.fill_(dg.DG_PHASE_DENOISE)
+    st.temperature.fill_(T)
+    st.request_id.copy_(torch.arange(B, device=dev) + rank * B)
+    ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device=dev)
+    out = torch.empty((B * C, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(lg):
+        dg.dg_denoise_step(p, lg, st, ws)
+        dg.dg_selfcond_embed(p, lg, st, E, out, ws)
+
+    for _ in range(args.warmup):
+        step(logits)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(gpu_id_for(dev))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for k in range(K):
+        ev[k][0].record(stream)
+        dg.dg_denoise_step(p, logits, st, ws)
+        ev[k][1].record(stream)
+        dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+        ev[k][2].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    ms_sampler = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    ms_sc = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    status = int(st.device_status.item())
+
+    # end-to-end: host logits in pinned memory copied in, results copied out
+    host_logits = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+    host_logits.copy_(logits)
+    dev_logits = torch.empty_like(logits)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_canvas = torch.empty(st.canvas.shape, dtype=st.canvas.dtype, pin_memory=True)
+    for _ in range(max(1, args.warmup)):
+        dev_logits.copy_(host_logits, non_blocking=True)
+        step(dev_logits)
+        host_out.copy_(out, non_blocking=True)
+        host_canvas.copy_(st.canvas, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    Ke = max(1, K // 4)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        dev_logits.copy_(host_logits, non_blocking=True)
+        step(dev_logits)
+        host_out.copy_(out, non_blocking=True)
+        host_canvas.copy_(st.canvas, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e0.elapsed_time(e1)
+
+    if world > 1:
+        tm = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms, ms_e2e = float(tm[0]), float(tm[1])
+
+    if rank != 0:
+        return None
+    n_pos = B * C
+    value = world * n_pos * K / (ms / 1e3)
+    e2e_value = world * n_pos * Ke / (ms_e2e / 1e3)
+    hbm, bf16, src = peaks()
+    flops = 2.0 * n_pos * V * d
+    sc_tflops = flops / (ms_sc / 1e3) / 1e12
+    logit_bytes = n_pos * V * esz
+    sampler_gbs = logit_bytes / (ms_sampler / 1e3) / 1e9
+    from denoise_step_sampler_gb300 import build as _b  # noqa: F401
+    plan_splits = _selfcond_splits(n_pos, V, d)
+    launches_per_step = 2 + 1 + (1 if plan_splits > 1 else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt,
+        "data": "synthetic (seeded Gaussian logits + one boosted token per position; E ~ N(0,0.02^2))",
+        "config": {"workload": args.workload if not args.batch else f"{B}x256 ({args.workload} shape)",
+                   "batch_canvases": B, "canvas_len": C, "vocab": V, "d": d, "temperature": T,
+                   "entropy_budget": budget, "logits_bytes": logit_bytes,
+                   "l2": "inputs larger than L2 (logits %.2f GB, E %.2f GB); no flush" % (
+                       logit_bytes / 1e9, V * d * 2 / 1e9),
+                   "parallelism": f"replicas x{world} (independent requests per GPU)"},
+        "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
+                     "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
+                     "frac": sc_tflops / bf16, "traffic": None,
+                     "peak_source": f"{src} bf16 burst", "flops_per_launch": flops,
+                     "ms_per_launch": ms_sc},
+        "roofline_sampler": {"bound": "hbm", "kernel": "dg_denoise_step (vocab pass + canvas step)",
+                             "achieved": sampler_gbs, "peak": hbm, "unit": "GB/s",
+                             "frac": sampler_gbs / hbm, "traffic": None,
+                             "peak_source": f"{src} copy", "bytes_per_launch": logit_bytes,
+                             "ms_per_launch": ms_sampler},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "positions/s",
+                "h2d_bytes_per_step": logit_bytes,
+                "d2h_bytes_per_step": int(out.numel() * 4 + st.canvas.numel() * 4),
+                "steps": Ke},
+        "gpu_launches": launches_per_step * K,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        try:
+            cb = cpu_baseline_subprocess(args.workload if not args.batch else DEFAULT)
+            line["cpu_baseline"] = {"value": cb["value"], "unit": "positions/s", "cores": 1,
+                                    "kind": "oracle", "sample": cb["sample"]}
+        except Exception as e:  # pragma: no cover
+            line["cpu_baseline"] = {"value": None, "error": str(e)[:300]}
+    return line
+
+
+def _selfcond_splits(rows, V, d):
+    # mirrors the library's plan only to count launches (it does not affect timing)
+    BM, BN, BK, SMS = 128, 256, 64, 152
+    m, n, k = -(-rows // BM), -(-d // BN), -(-V // BK)
+    tiles = m * n
+    best, best_eff = 1, 0.0
+    for sp in range(1, 33):
+        if sp > 1 and k // sp < 8:
+            break
+        ctas = tiles * sp
+        waves = -(-ctas // SMS)
+        eff = ctas / (waves * SMS)
+        if eff > best_eff + 0.05:
+            best, best_eff = sp, eff
+    kbps = -(-k // best)
+    return -(-k // kbps)
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    B, C, V, dt, T, budget, d, boost = WORKLOADS[args.workload]
+    # each step: a bounded sample sized so the whole run takes ~2-3 minutes
+    per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))
+    rate, P, t = cpu_oracle_sample(args.workload, per_step, max_positions=None)
+    # warm-up + timed steps on the same sample size
+    import torch
+    from denoise_step_sampler_gb300 import synthetic as syn
+    from oracle import sampler as osam
+    from oracle import selfcond as osc
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    z = syn.boosted_logits(P, V, seed=SEED, dtype=tdt, device="cpu", boost_hi=boost).float().numpy()
+    E = syn.embedding(V, d, seed=SEED, device="cpu").float().numpy().astype(np.float64)
+    Tf = float(np.float32(T))
+
+    def one():
+        H = []
+        for i in range(P):
+            ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
+            H.append(osam.vocab_pass(z[i].astype(np.float64), Tf, ka, kb, kc).entropy)
+        osam.accept_mask(np.resize(np.asarray(H), C), budget)
+        osc.selfcond_rows(z.astype(np.float64), Tf, E)
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    el = time.perf_counter() - t0
+    value = P * args.steps / el
+    sample = f"{P} position(s) of canvas 0 per step: vocab pass + self-cond row(s), fp64"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "positions/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "batch_canvases": B, "canvas_len": C, "vocab": V,
+                   "d": d},
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": _threads_used(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def _threads_used() -> int:
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(k)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--batch", type=int, default=0, help="override the canvas count (sweep)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-oracle-leg", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.cpu_oracle_leg:
+        rate, P, t = cpu_oracle_sample(args.workload, args.cpu_budget)
+        print(json.dumps({"value": rate, "positions": P, "seconds": t,
+                          "sample": f"{P} positions of canvas 0 of the same workload: vocab pass "
+                                    f"+ self-cond rows (fp64 numpy, 1 thread), {t:.1f} s"}))
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line))
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    line = run_ours(args, rank, world, dev)
+    if line is not None:
+        print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+// C-ABI front end: argument validation (no side effect on failure), the
+// workspace query, and the launches of the sampler kernels on the caller's
+// stream.  Nothing here allocates, frees or synchronises.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+using namespace dg;
+
+namespace {
+
+bool params_ok(const dg_params *p) {
+  if (!p) return false;
+  if (p->batch < 1 || p->canvas_len < 1 || p->canvas_len > 1024) return false;
+  if (p->vocab < 2) return false;
+  if (p->logits_dtype != DG_F32 && p->logits_dtype != DG_BF16) return false;
+  if (p->logits_ld < p->vocab) return false;
+  if (!std::isfinite(p->entropy_budget) || p->entropy_budget < 0.f) return false;
+  if (std::isnan(p->conf_threshold)) return false;
+  if (p->stable_k < 1 || p->step_cap < 1) return false;
+  // positions and partial records must be addressable
+  const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
+  if (n_pos > ((int64_t)1 << 40)) return false;
+  return true;
+}
+
+bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t denoise_ws_bytes(const dg_params *p) {
+  const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
+  const VocabChunking vc = vocab_chunking(n_pos, p->vocab);
+  return round_up((size_t)n_pos * (size_t)vc.n_chunks * sizeof(Partial), 256);
+}
+
+// The device must be an sm_103 part (GB300); checked once per device.
+int device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  static int cache[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? DG_OK : DG_ERR_UNSUPPORTED;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  return ok ? DG_OK : DG_ERR_UNSUPPORTED;
+}
+
+bool state_ok_phase_machine(const dg_state *st) {
+  return st && st->phase && st->request_id && st->rng_step && st->step && st->stable &&
+         st->canvas && st->converged && st->sc_valid && st->num_sampled && st->num_rejected &&
+         st->device_status;
+}
+
+bool state_ok_full(const dg_state *st) {
+  return state_ok_phase_machine(st) && st->temperature && st->argmax_prev && st->cand &&
+         st->argmax && st->accept && st->m && st->s && st->entropy && st->mean_entropy &&
+         st->emitted;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dg_workspace_bytes(const dg_params *p, int32_t d) {
+  if (!params_ok(p) || d < 0) return 0;
+  size_t ws = denoise_ws_bytes(p);
+  if (d > 0) {
+    const SelfcondPlan pl = selfcond_plan((int64_t)p->batch * p->canvas_len, p->vocab, d);
+    if (pl.ws_bytes > ws) ws = pl.ws_bytes;
+  }
+  return ws;
+}
+
+int dg_init_canvas(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
+                   cudaStream_t stream) {
+  if (!params_ok(p) || !state_ok_phase_machine(st) || !row_mask) return DG_ERR_INVALID_ARG;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  cudaGetLastError();
+  if (launch_canvas_step(*p, *st, nullptr, 0, 1, row_mask, stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
+int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
+              cudaStream_t stream) {
+  if (!params_ok(p) || !state_ok_phase_machine(st) || !row_mask || !st->argmax_prev ||
+      !st->emitted)
+    return DG_ERR_INVALID_ARG;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  cudaGetLastError();
+  if (launch_canvas_step(*p, *st, nullptr, 0, 2, row_mask, stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
+int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st, void *ws,
+                    size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p) || !state_ok_full(st) || !logits) return DG_ERR_INVALID_ARG;
+  const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return DG_ERR_INVALID_ARG;
+  const size_t need = denoise_ws_bytes(p);
+  if (!ws || ws_bytes < need || !aligned(ws, 16)) return DG_ERR_WORKSPACE;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  cudaGetLastError();
+  const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
+  const VocabChunking vc = vocab_chunking(n_pos, p->vocab);
+  Partial *part = reinterpret_cast<Partial *>(ws);
+  if (launch_vocab_pass(*p, logits, *st, part, vc.chunk, vc.n_chunks, stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (launch_canvas_step(*p, *st, part, vc.n_chunks, 0, nullptr, stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
+int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st, const void *E,
+                      int32_t d, int64_t ld_E, void *out, int32_t out_dtype, void *ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+  if (!params_ok(p) || !st || !logits || !E || !out) return DG_ERR_INVALID_ARG;
+  if (!st->phase || !st->sc_valid || !st->temperature || !st->m || !st->s || !st->device_status)
+    return DG_ERR_INVALID_ARG;
+  if (d < 16 || d % 16 != 0 || ld_E < d || (ld_E * 2) % 16 != 0) return DG_ERR_INVALID_ARG;
+  if (out_dtype != DG_F32 && out_dtype != DG_BF16) return DG_ERR_INVALID_ARG;
+  const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
+  if (!aligned(logits, esz) || !aligned(E, 16) || !aligned(out, 16)) return DG_ERR_INVALID_ARG;
+  const int64_t rows = (int64_t)p->batch * p->canvas_len;
+  const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d);
+  if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned(ws, 16)))
+    return DG_ERR_WORKSPACE;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  cudaGetLastError();
+  if (launch_selfcond(*p, logits, *st, E, d, ld_E, out, out_dtype, ws, pl, stream) !=
+      cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
+const char *dg_status_string(int code) {
+  switch (code) {
+    case DG_OK:
+      return "ok";
+    case DG_ERR_INVALID_ARG:
+      return "invalid argument";
+    case DG_ERR_UNSUPPORTED:
+      return "unsupported device or configuration (needs sm_103)";
+    case DG_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    case DG_ERR_CUDA:
+      return "CUDA error";
+    default:
+      return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,272 @@
+// K2 -- one CTA per request slot: the per-canvas half of the sampler step.
+//
+// DENOISE rows: merge the vocabulary-pass partials of each position into
+// (m, s, H, argmax, cand); sort the canvas's (H, i) pairs ascending with a
+// bitonic network in shared memory; exclusive prefix sum of the sorted
+// entropies in fp64; accept while it stays within the budget (the first
+// always) -- "DiffusionGemma Explained", section "Sampling", step 3; re-noise
+// rejected positions to uniform tokens (Technical Report section 3.3); the
+// convergence test and phase update (vLLM blog, "Entropy-bounded denoising"
+// and "Putting it together").
+// PREFILL rows: a fresh uniform canvas.  COMMIT rows: emit the clean argmax
+// canvas, then a fresh canvas and reset counters.  IDLE rows: untouched.
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int kMaxC = 1024;
+
+__device__ __forceinline__ double warp_incl_scan(double x, int lane) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const double y = __shfl_up_sync(0xFFFFFFFFu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x;
+}
+
+__device__ __forceinline__ double warp_sum(double x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  return x;
+}
+
+struct CanvasArgs {
+  int32_t B, C, V;
+  uint64_t seed;
+  float budget, thr;
+  int32_t stable_k, step_cap;
+  dg_state st;
+  const Partial *part;
+  int32_t n_chunks;
+  int mode;
+  const uint8_t *row_mask;
+};
+
+__global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
+  __shared__ float skey[kMaxC];
+  __shared__ int32_t sidx[kMaxC];
+  __shared__ uint8_t sacc[kMaxC];
+  __shared__ double swarp[32];
+  __shared__ double soff[32];
+
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+  const int C = a.C, V = a.V;
+  const dg_state &st = a.st;
+
+  const uint8_t ph = st.phase[r];
+  bool do_init = false, do_commit = false;
+  if (a.mode == 0) {
+    if (ph == DG_PHASE_IDLE) return;
+    if (ph > DG_PHASE_IDLE) {
+      if (tid == 0) atomicOr(st.device_status, (uint32_t)DG_DEV_BAD_PHASE);
+      return;
+    }
+    do_init = (ph == DG_PHASE_PREFILL);
+    do_commit = (ph == DG_PHASE_COMMIT);
+  } else {
+    if (!a.row_mask[r]) return;
+    do_init = (a.mode == 1);
+    do_commit = (a.mode == 2);
+  }
+  const uint64_t rid = st.request_id[r];
+  const uint64_t rs = st.rng_step[r];
+  const int64_t base = (int64_t)r * C;
+
+  if (do_init || do_commit) {
+    for (int i = tid; i < C; i += nt) {
+      if (do_commit) {
+        int32_t tok = st.argmax_prev[base + i];
+        if (tok < 0 || tok >= V) {
+          atomicOr(st.device_status, (uint32_t)DG_DEV_BAD_TOKEN);
+          tok = 0;
+        }
+        st.emitted[base + i] = tok;
+      }
+      const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)i);
+      st.canvas[base + i] =
+          (int32_t)below((uint32_t)(stream_key(pk, kTagInit) >> 32), (uint32_t)V);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      st.step[r] = 0;
+      st.stable[r] = 0;
+      st.num_sampled[r] = do_commit ? C : 0;
+      st.num_rejected[r] = 0;
+      st.sc_valid[r] = 0;
+      st.converged[r] = 0;
+      st.phase[r] = DG_PHASE_DENOISE;
+      st.rng_step[r] = rs + 1;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ DENOISE
+  const float T = st.temperature[r];
+  const float c = kLog2e / T;
+  bool valid = false;
+  float H = NAN;
+  int32_t am = 0, cand = 0;
+  if (tid < C) {
+    const Partial *P = a.part + (size_t)(base + tid) * a.n_chunks;
+    uint32_t fl = 0;
+    float zmax = -INFINITY, b2 = -INFINITY;
+    int32_t pam = -1, pcand = -1;
+    for (int ch = 0; ch < a.n_chunks; ++ch) {
+      const Partial q = P[ch];
+      fl |= q.flags;
+      if (q.zmax > zmax || (q.zmax == zmax && q.am >= 0 && (pam < 0 || q.am < pam))) {
+        zmax = q.zmax;
+        pam = q.am;
+      }
+      if (q.b2 > b2 || (q.b2 == b2 && q.cand >= 0 && (pcand < 0 || q.cand < pcand))) {
+        b2 = q.b2;
+        pcand = q.cand;
+      }
+    }
+    float m_out = NAN, s_out = NAN;
+    if (!(fl & (kPartNaN | kPartPInf | kPartBadT)) && zmax != -INFINITY && pam >= 0 &&
+        pcand >= 0) {
+      const double M2 = (double)(zmax * c);
+      double S = 0.0, Tt = 0.0;
+      for (int ch = 0; ch < a.n_chunks; ++ch) {
+        const Partial q = P[ch];
+        if (q.s > 0.f) {
+          const double d = (double)(q.zmax * c) - M2;
+          const double f = exp2(d);
+          S += (double)q.s * f;
+          Tt += ((double)q.t + d * (double)q.s) * f;
+        }
+      }
+      if (S > 0.0 && isfinite(S) && isfinite(Tt)) {
+        valid = true;
+        H = (float)(0.6931471805599453 * (log2(S) - Tt / S));
+        m_out = zmax / T;
+        s_out = (float)S;
+        am = pam;
+        cand = pcand;
+      }
+    }
+    if (!valid && !(fl & kPartBadT)) atomicOr(st.device_status, (uint32_t)DG_DEV_NONFINITE_LOGITS);
+    st.m[base + tid] = m_out;
+    st.s[base + tid] = s_out;
+    st.entropy[base + tid] = H;
+    st.argmax[base + tid] = am;
+    st.cand[base + tid] = cand;
+  }
+
+  // sort (H, i) ascending; invalid positions and padding sort last as +inf
+  skey[tid] = valid ? H : INFINITY;
+  sidx[tid] = tid;
+  __syncthreads();
+  for (int k = 2; k <= nt; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int o = tid ^ j;
+      if (o > tid) {
+        const float ka = skey[tid], kb = skey[o];
+        const int32_t ia = sidx[tid], ib = sidx[o];
+        const bool gt = (ka > kb) || (ka == kb && ia > ib);
+        const bool up = ((tid & k) == 0);
+        if (gt == up) {
+          skey[tid] = kb;
+          skey[o] = ka;
+          sidx[tid] = ib;
+          sidx[o] = ia;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // exclusive prefix sum of the sorted entropies (fp64), then the budget rule
+  const double x = (double)skey[tid];
+  const double incl = warp_incl_scan(x, lane);
+  double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (lane == 0) excl = 0.0;
+  if (lane == 31) swarp[warp] = incl;
+  __syncthreads();
+  if (tid == 0) {
+    double run = 0.0;
+    for (int w = 0; w < nwarps; ++w) {
+      soff[w] = run;
+      run += swarp[w];
+    }
+  }
+  __syncthreads();
+  const double E = soff[warp] + excl;
+  const bool acc_k = isfinite(x) && (tid == 0 || E <= (double)a.budget);
+  sacc[sidx[tid]] = acc_k ? 1 : 0;
+  __syncthreads();
+
+  // re-noise, accept mask, convergence
+  int same = 1;
+  double hsum = 0.0;
+  if (tid < C) {
+    const bool acc = sacc[tid] != 0;
+    st.accept[base + tid] = acc ? 1 : 0;
+    int32_t tok = cand;
+    if (!acc) {
+      const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)tid);
+      tok = (int32_t)below((uint32_t)(stream_key(pk, kTagRenoise) >> 32), (uint32_t)V);
+    }
+    st.canvas[base + tid] = tok;
+    same = (st.argmax_prev[base + tid] == am) ? 1 : 0;
+    st.argmax_prev[base + tid] = am;
+    hsum = valid ? (double)H : (double)NAN;
+  }
+  const int all_same = __syncthreads_and(same);
+  const double wsum = warp_sum(hsum);
+  if (lane == 0) swarp[warp] = wsum;
+  __syncthreads();
+  if (tid == 0) {
+    double tot = 0.0;
+    for (int w = 0; w < nwarps; ++w) tot += swarp[w];
+    const double hbar = tot / (double)C;
+    const int32_t step0 = st.step[r];
+    const bool same_row = (step0 > 0) && all_same;
+    const int32_t stable = same_row ? st.stable[r] + 1 : 0;
+    const int32_t step1 = step0 + 1;
+    const bool conv = (stable >= a.stable_k && hbar < (double)a.thr) || step1 >= a.step_cap;
+    st.stable[r] = stable;
+    st.step[r] = step1;
+    st.mean_entropy[r] = (float)hbar;
+    st.converged[r] = conv ? 1 : 0;
+    st.sc_valid[r] = conv ? 0 : 1;
+    st.phase[r] = conv ? DG_PHASE_COMMIT : DG_PHASE_DENOISE;
+    st.num_sampled[r] = 0;
+    st.num_rejected[r] = C;
+    st.rng_step[r] = rs + 1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Partial *part,
+                               int32_t n_chunks, int mode, const uint8_t *row_mask,
+                               cudaStream_t s) {
+  int threads = 32;
+  while (threads < p.canvas_len) threads <<= 1;
+  CanvasArgs a;
+  a.B = p.batch;
+  a.C = p.canvas_len;
+  a.V = p.vocab;
+  a.seed = p.seed;
+  a.budget = p.entropy_budget;
+  a.thr = p.conf_threshold;
+  a.stable_k = p.stable_k;
+  a.step_cap = p.step_cap;
+  a.st = st;
+  a.part = part;
+  a.n_chunks = n_chunks;
+  a.mode = mode;
+  a.row_mask = row_mask;
+  canvas_step_kernel<<<p.batch, threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,127 @@
+// Device-side building blocks shared by the library's kernels: the counter
+// hash (SplitMix64 output function, MurmurHash3 fmix32), the Exp(1) draws,
+// the vocabulary-pass partial record, and small PTX wrappers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dg.h"
+
+namespace dg {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kGroup = 8;  // vocabulary indices per Gumbel group
+
+enum : uint32_t { kTagGMin = 1, kTagGArg = 2, kTagGRest = 3, kTagRenoise = 4, kTagInit = 5 };
+
+// SplitMix64 output function of the state x (Steele, Lea & Flood 2014).
+__host__ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
+  uint64_t z = x + 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+// MurmurHash3 32-bit finalizer.
+__host__ __device__ __forceinline__ uint32_t fmix32(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85EBCA6Bu;
+  h ^= h >> 13;
+  h *= 0xC2B2AE35u;
+  h ^= h >> 16;
+  return h;
+}
+
+// Key of (seed, request, rng_step, position); stream keys append the tag.
+__device__ __forceinline__ uint64_t position_key(uint64_t seed, uint64_t req, uint64_t rstep,
+                                                 uint64_t pos) {
+  uint64_t k = mix64(seed);
+  k = mix64(k ^ req);
+  k = mix64(k ^ rstep);
+  return mix64(k ^ pos);
+}
+__device__ __forceinline__ uint64_t stream_key(uint64_t pkey, uint32_t tag) {
+  return mix64(pkey ^ (uint64_t)tag);
+}
+
+// floor(h * n / 2^32): an integer uniform in [0, n).
+__device__ __forceinline__ uint32_t below(uint32_t h, uint32_t n) {
+  return (uint32_t)(((uint64_t)h * (uint64_t)n) >> 32);
+}
+
+// -ln((h + 1/2) / 2^32); the upper half goes through log1p of the exact
+// complement so that small values keep their relative precision.
+__device__ __forceinline__ float exp1_draw(uint32_t h) {
+  if (h < 0x80000000u) {
+    const float u = fmaf((float)h, 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+    return -logf(u);
+  }
+  const float w = fmaf((float)(~h), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+  return -log1pf(-w);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Packed pairs of fp32 (Blackwell f32x2 arithmetic).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  return ((uint64_t)__float_as_uint(hi) << 32) | (uint64_t)__float_as_uint(lo);
+}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Per (position, vocabulary chunk) result of the vocabulary pass.
+//   zmax/am : largest stored logit of the chunk and its lowest index (-1 none)
+//   s, t    : sum 2^a and sum a 2^a, a = z*c - fl(zmax*c), c = log2(e)/T
+//   b2/cand : best perturbed score (z*c - log2 E) and its lowest index
+//   flags   : kPartNaN / kPartPInf / kPartBadT
+struct alignas(16) Partial {
+  float zmax;
+  int32_t am;
+  float s;
+  float t;
+  float b2;
+  int32_t cand;
+  uint32_t flags;
+  uint32_t pad;
+};
+enum : uint32_t { kPartNaN = 1u, kPartPInf = 2u, kPartBadT = 4u };
+
+// Chunking of the vocabulary for the vocabulary pass: a pure function of the
+// sizes, shared by the workspace query and the launch.
+struct VocabChunking {
+  int32_t chunk;     // elements per chunk (multiple of 256 unless one chunk)
+  int32_t n_chunks;  // chunks per position
+};
+__host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V) {
+  // Aim for ~16K warps in flight over the whole launch; never below 2048
+  // elements per warp so that the per-warp set-up stays amortised.
+  const int64_t target_warps = 16384;
+  int64_t want = (target_warps + n_pos - 1) / n_pos;
+  int64_t nc = 1;
+  while (nc < want && nc < 256) nc <<= 1;
+  while (nc > 1 && ((int64_t)V + nc - 1) / nc < 2048) nc >>= 1;
+  int64_t chunk = ((int64_t)V + nc - 1) / nc;
+  chunk = (chunk + 255) / 256 * 256;
+  VocabChunking out;
+  out.chunk = (int32_t)chunk;
+  out.n_chunks = (int32_t)(((int64_t)V + chunk - 1) / chunk);
+  return out;
+}
+
+}  // namespace dg

@@ -1,0 +1,39 @@
+// Host-side launchers shared between the C-ABI front end (dg_api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dg.h"
+
+namespace dg {
+
+struct Partial;
+
+// K1: fused vocabulary pass -> per (position, chunk) partial records.
+cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_state &st,
+                              Partial *part, int32_t chunk, int32_t n_chunks, cudaStream_t s);
+
+// K2: per-canvas merge + acceptance + re-noise + convergence + phase machine.
+// mode 0: every row by its phase; 1: init rows in row_mask; 2: commit rows in row_mask.
+cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Partial *part,
+                               int32_t n_chunks, int mode, const uint8_t *row_mask,
+                               cudaStream_t s);
+
+// K4: self-conditioning GEMM (tcgen05 / TMEM).
+struct SelfcondPlan {
+  int32_t m_tiles;   // ceil(B*C / 128)
+  int32_t n_tiles;   // ceil(d / BN)
+  int32_t splits;    // K splits over the vocabulary
+  int32_t k_blocks;  // ceil(V / BK)
+  int32_t kb_per_split;  // k-blocks per split (every split non-empty)
+  size_t ws_bytes;   // split-K partial sums (0 if splits == 1)
+};
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d);
+cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
+                            const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
+                            void *ws, const SelfcondPlan &plan, cudaStream_t s);
+
+}  // namespace dg

@@ -1,0 +1,563 @@
+// K4 -- the self-conditioning contraction out = softmax(z/T) . E on the
+// Blackwell tensor cores (Technical Report section 3.2, eq. 6: the p0 E inside
+// FFW(p0 E)).
+//
+// The probabilities are never stored: producer warps rebuild each 128 x 64
+// bf16 tile of p from the logits and the per-position (m, s) written by the
+// sampler step, p = 2^(z*log2(e)/T - (m*log2(e) + log2 s)), and write it into
+// shared memory in the 128-byte-swizzled K-major layout the MMA reads.  The
+// E tile (64 vocabulary rows x 256 embedding columns, bf16, N-major) arrives
+// by TMA.  One thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 ->
+// fp32) into a TMEM accumulator; the epilogue reads it back with tcgen05.ld.
+// Small batches split the vocabulary (K) across CTAs and reduce the fp32
+// partial sums in a second kernel.  Every wait is bounded: a wait that gives up
+// sets DG_DEV_WAIT_TIMEOUT, the CTA drains what it issued and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int NST = 4;
+constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 producers/epilogue
+constexpr int kProdWarps = 4;
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
+constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + 2048 + 1024;
+constexpr int kAssumedSMs = 152;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+
+struct Shared {
+  uint64_t full_a[NST];
+  uint64_t full_b[NST];
+  uint64_t empty[NST];
+  uint64_t tmem_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int32_t abort_flag;
+  int32_t any_valid;
+  float row_c[BM];
+  float row_l2[BM];
+  int32_t row_ok[BM];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false if it gave up or another role aborted.
+__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Shared *sh,
+                                       uint32_t *status) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(b, parity)) {
+    if (*(volatile int32_t *)&sh->abort_flag) return false;
+    if (globaltimer() - t0 > kWaitNs) {
+      *(volatile int32_t *)&sh->abort_flag = 1;
+      atomicOr(status, (uint32_t)DG_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+// Bounded wait used while draining after an abort (ignores the abort flag).
+__device__ __noinline__ void mbar_drain(uint64_t *b, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try(b, parity)) {
+    if (globaltimer() - t0 > kWaitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B N-major, M=128, N=BN.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+struct GemmArgs {
+  const void *logits;
+  int64_t ld;
+  int32_t V, C, d, dtype;
+  int64_t rows;  // B*C
+  int32_t n_tiles, splits, k_blocks, kb_per_split;
+  const uint8_t *phase;
+  const uint8_t *sc_valid;
+  const float *temperature;
+  const float *m;
+  const float *s;
+  void *out;
+  int32_t out_dtype;
+  float *partial;  // [splits][rows][d] when splits > 1
+  uint32_t *status;
+};
+
+__device__ __forceinline__ bool row_feeds(const GemmArgs &a, int64_t q, float &c, float &l2) {
+  if (q >= a.rows) return false;
+  const int64_t r = q / a.C;
+  if (a.sc_valid[r] != 1 || a.phase[r] != DG_PHASE_DENOISE) return false;
+  const float m = a.m[q], s = a.s[q], T = a.temperature[r];
+  if (!(isfinite(m) && s > 0.f && isfinite(s) && T > 0.f && isfinite(T))) return false;
+  c = kLog2e / T;
+  l2 = fmaf(m, kLog2e, __log2f(s));
+  return true;
+}
+
+// Load 8 consecutive logits of row `row` starting at column k (columns >= V
+// read as -inf, i.e. probability 0).
+__device__ __forceinline__ void load8(const GemmArgs &a, const char *rowp, bool vec_ok, int64_t k,
+                                      float (&z)[8]) {
+  if (vec_ok && k + 8 <= a.V) {
+    if (a.dtype == DG_BF16) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rowp + k * 2));
+      z[0] = __uint_as_float(v.x << 16);
+      z[1] = __uint_as_float(v.x & 0xFFFF0000u);
+      z[2] = __uint_as_float(v.y << 16);
+      z[3] = __uint_as_float(v.y & 0xFFFF0000u);
+      z[4] = __uint_as_float(v.z << 16);
+      z[5] = __uint_as_float(v.z & 0xFFFF0000u);
+      z[6] = __uint_as_float(v.w << 16);
+      z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+    } else {
+      const float4 u = __ldg(reinterpret_cast<const float4 *>(rowp + k * 4));
+      const float4 w = __ldg(reinterpret_cast<const float4 *>(rowp + k * 4 + 16));
+      z[0] = u.x; z[1] = u.y; z[2] = u.z; z[3] = u.w;
+      z[4] = w.x; z[5] = w.y; z[6] = w.z; z[7] = w.w;
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int64_t kk = k + j;
+    if (kk < a.V) {
+      if (a.dtype == DG_BF16)
+        z[j] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(rowp) + kk)
+                               << 16);
+      else
+        z[j] = __ldg(reinterpret_cast<const float *>(rowp) + kk);
+    } else {
+      z[j] = -INFINITY;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e, GemmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint8_t *sA = smem;                    // NST x 16 KB
+  uint8_t *sB = smem + NST * kABytes;    // NST x 32 KB
+  Shared *sh = reinterpret_cast<Shared *>(smem + NST * (kABytes + kBBytes));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x;
+  const int n_t = tile % a.n_tiles;
+  const int rest = tile / a.n_tiles;
+  const int m_t = rest % (int)((a.rows + BM - 1) / BM);
+  const int split = rest / (int)((a.rows + BM - 1) / BM);
+  const int64_t row0 = (int64_t)m_t * BM;
+  const int n0 = n_t * BN;
+  const int kb0 = split * a.kb_per_split;
+  const int kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
+  const int nkb = max(0, kb1 - kb0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&sh->full_a[s], kProdWarps);
+      mbar_init(&sh->full_b[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    mbar_init(&sh->tmem_full, 1);
+    mbar_init(&sh->mma_done, 1);
+    sh->abort_flag = 0;
+    sh->any_valid = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;  // 0..127
+    float c = 0.f, l2 = 0.f;
+    const bool ok = row_feeds(a, row0 + t, c, l2);
+    sh->row_c[t] = c;
+    sh->row_l2[t] = l2;
+    sh->row_ok[t] = ok ? 1 : 0;
+    if (ok) atomicOr(&sh->any_valid, 1);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&sh->tmem_base)),
+                 "r"(BN));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+  const bool run = sh->any_valid != 0 && nkb > 0;
+
+  if (run) {
+    if (warp == 0) {
+      // ------------------------------------------------ TMA producer (E tiles)
+      if (lane == 0) {
+        int issued = 0;
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NST;
+          const uint32_t use = (uint32_t)(i / NST);
+          if (i >= NST && !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status)) break;
+          mbar_expect_tx(&sh->full_b[s], kBBytes);
+          uint8_t *dst = sB + s * kBBytes;
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_2d(dst + j * (BK * 128), &tmap_e, &sh->full_b[s], n0 + j * 64,
+                        (kb0 + i) * BK);
+          issued = i + 1;
+        }
+        // drain: every issued copy must land before the CTA may exit
+        for (int i = max(0, issued - NST); i < issued; ++i)
+          mbar_drain(&sh->full_b[i % NST], (uint32_t)(i / NST) & 1u);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NST;
+          const uint32_t par = (uint32_t)(i / NST) & 1u;
+          if (!mbar_wait(&sh->full_b[s], par, sh, a.status)) break;
+          if (!mbar_wait(&sh->full_a[s], par, sh, a.status)) break;
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + s * kABytes);
+          const uint32_t b_base = smem_u32(sB + s * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(b_base + kk * 2048, BK * 128, 1024);
+            mma_bf16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sh->empty[s]);
+        }
+        mma_commit(&sh->tmem_full);
+        mma_commit(&sh->mma_done);
+      }
+    } else {
+      // ------------------------------------------------ p producers
+      const int pw = warp - 2;  // 0..3
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % NST;
+        const uint32_t use = (uint32_t)(i / NST);
+        if (i >= NST && !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status)) break;
+        uint8_t *tileA = sA + s * kABytes;
+        const int64_t k0 = (int64_t)(kb0 + i) * BK;
+        const int chunk = lane & 7;
+#pragma unroll 2
+        for (int it = 0; it < 8; ++it) {
+          const int r = pw * 32 + it * 4 + (lane >> 3);
+          uint4 packed = make_uint4(0u, 0u, 0u, 0u);
+          if (sh->row_ok[r]) {
+            const int64_t q = row0 + r;
+            const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
+            const char *rowp =
+                reinterpret_cast<const char *>(a.logits) + (size_t)q * (size_t)a.ld * esz;
+            const bool vec_ok = ((reinterpret_cast<uintptr_t>(rowp) & 15u) == 0);
+            float z[8];
+            load8(a, rowp, vec_ok, k0 + chunk * 8, z);
+            const float c = sh->row_c[r], l2 = sh->row_l2[r];
+            float p[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) p[j] = ex2_approx(fmaf(z[j], c, -l2));
+            packed.x = pack_bf16x2(p[0], p[1]);
+            packed.y = pack_bf16x2(p[2], p[3]);
+            packed.z = pack_bf16x2(p[4], p[5]);
+            packed.w = pack_bf16x2(p[6], p[7]);
+          }
+          const uint32_t off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
+          *reinterpret_cast<uint4 *>(tileA + off) = packed;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->full_a[s]);
+      }
+    }
+  }
+
+  // ---------------------------------------------------- epilogue
+  if (warp >= 2) {
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;
+    const int64_t q = row0 + r;
+    bool have = false;
+    if (run) have = mbar_wait(&sh->tmem_full, 0, sh, a.status);
+    have = __all_sync(0xFFFFFFFFu, have);
+    tc_fence_after();
+    const bool ok = have && sh->row_ok[r] != 0;
+    for (int cb = 0; cb < BN; cb += 32) {
+      float v[32];
+      if (have) {
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cb, v);
+      }
+      if (q >= a.rows) continue;
+      const int col0 = n0 + cb;
+      if (col0 >= a.d) continue;
+      const int ncol = min(32, a.d - col0);
+      if (!ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      if (a.splits > 1) {
+        if (!run) continue;  // the reduction writes zeros for rows that do not feed
+        float *dst = a.partial + ((size_t)split * a.rows + q) * a.d + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (j < ncol) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      } else if (a.out_dtype == DG_F32) {
+        float *dst = reinterpret_cast<float *>(a.out) + (size_t)q * a.d + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          if (j < ncol) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      } else {
+        __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.out) + (size_t)q * a.d + col0;
+#pragma unroll
+        for (int j = 0; j < 32; j += 8)
+          if (j < ncol)
+            *reinterpret_cast<uint4 *>(dst + j) =
+                make_uint4(pack_bf16x2(v[j], v[j + 1]), pack_bf16x2(v[j + 2], v[j + 3]),
+                           pack_bf16x2(v[j + 4], v[j + 5]), pack_bf16x2(v[j + 6], v[j + 7]));
+      }
+    }
+  }
+
+  // ---------------------------------------------------- teardown
+  if (run && warp == 1 && lane == 0) mbar_drain(&sh->mma_done, 0);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN));
+  }
+}
+
+// out[q, :] = sum over splits of the partial sums, zeros for rows that do
+// not feed the next step.
+__global__ void selfcond_reduce_kernel(GemmArgs a) {
+  const int64_t n4 = a.rows * (int64_t)(a.d / 4);
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n4;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t q = e / (a.d / 4);
+    const int64_t col = (e - q * (a.d / 4)) * 4;
+    float c, l2;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row_feeds(a, q, c, l2)) {
+      for (int sp = 0; sp < a.splits; ++sp) {
+        const float4 v =
+            *reinterpret_cast<const float4 *>(a.partial + ((size_t)sp * a.rows + q) * a.d + col);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+    }
+    if (a.out_dtype == DG_F32) {
+      *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + q * a.d + col) = acc;
+    } else {
+      __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.out) + q * a.d + col;
+      *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(acc.x, acc.y);
+      *reinterpret_cast<uint32_t *>(dst + 2) = pack_bf16x2(acc.z, acc.w);
+    }
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
+  SelfcondPlan pl;
+  pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
+  pl.n_tiles = (d + BN - 1) / BN;
+  pl.k_blocks = (V + BK - 1) / BK;
+  const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
+  // Choose the split count whose CTA count fills the SMs best (waves of
+  // kAssumedSMs), keeping at least 8 k-blocks per split.
+  int best = 1;
+  double best_eff = 0.0;
+  for (int sp = 1; sp <= 32; ++sp) {
+    if (sp > 1 && pl.k_blocks / sp < 8) break;
+    const int64_t ctas = tiles * sp;
+    const int64_t waves = (ctas + kAssumedSMs - 1) / kAssumedSMs;
+    const double eff = (double)ctas / (double)(waves * kAssumedSMs);
+    if (eff > best_eff + 0.05) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  const int32_t kbps = (pl.k_blocks + best - 1) / best;
+  pl.kb_per_split = kbps;
+  pl.splits = (pl.k_blocks + kbps - 1) / kbps;
+  pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0;
+  return pl;
+}
+
+cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
+                            const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
+                            void *ws, const SelfcondPlan &plan, cudaStream_t s) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)BK};
+  const cuuint32_t estr[2] = {1, 1};
+  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(E), dims, strides, box,
+          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+
+  GemmArgs a;
+  a.logits = logits;
+  a.ld = p.logits_ld;
+  a.V = p.vocab;
+  a.C = p.canvas_len;
+  a.d = d;
+  a.dtype = p.logits_dtype;
+  a.rows = (int64_t)p.batch * p.canvas_len;
+  a.n_tiles = plan.n_tiles;
+  a.splits = plan.splits;
+  a.k_blocks = plan.k_blocks;
+  a.kb_per_split = plan.kb_per_split;
+  a.phase = st.phase;
+  a.sc_valid = st.sc_valid;
+  a.temperature = st.temperature;
+  a.m = st.m;
+  a.s = st.s;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.partial = reinterpret_cast<float *>(ws);
+  a.status = st.device_status;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(selfcond_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
+  selfcond_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (plan.splits > 1) {
+    const int64_t n4 = a.rows * (d / 4);
+    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+    selfcond_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace dg

@@ -1,0 +1,421 @@
+// K1 -- the fused vocabulary pass.
+//
+// One warp streams one contiguous chunk of one position's logit row exactly
+// once and produces, without materialising probabilities:
+//   * the clean argmax (largest stored logit, lowest index on ties);
+//   * the online-softmax pair (s, t) in base 2 relative to the running maximum,
+//     from which the entropy H = ln s - t/s follows ("DiffusionGemma
+//     Explained", section "Sampling", step 2);
+//   * the Gumbel-max candidate argmax(z/T + G) (vLLM blog, "Putting it
+//     together": argmax(logits/T + gumbel_noise)).
+// The Gumbel noise uses the library's exact group construction (8 indices per
+// group share one minimum draw), so the common path costs one hash per 16-byte
+// vector; a group is evaluated element by element only when it can still hold
+// the winner (group minimum X/8 <= e^{max y - best}).  Chunks that hold a NaN,
+// +inf or -inf logit are redone on a careful scalar path.
+#include <cuda_bf16.h>
+
+#include "dg_device.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int kWarps = 8;  // warps per CTA
+
+struct Keys {
+  uint32_t ka, kb, kc;  // low words of the GMIN / GARG / GREST stream keys
+};
+
+struct Lane {
+  float zmax;   // running max of stored logits
+  int32_t am;   // its lowest index
+  float m2;     // fl(zmax * c)
+  uint64_t S0, S1, T0, T1;  // packed partial sums of 2^a and a 2^a
+  float b2;     // best perturbed score, base 2
+  int32_t cand;
+};
+
+__device__ __forceinline__ void lane_init(Lane &L) {
+  L.zmax = -INFINITY;
+  L.am = -1;
+  L.m2 = -INFINITY;
+  L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+  L.b2 = -INFINITY;
+  L.cand = -1;
+}
+
+__device__ __forceinline__ void sums(const Lane &L, float &s, float &t) {
+  s = (lo2(L.S0) + hi2(L.S0)) + (lo2(L.S1) + hi2(L.S1));
+  t = (lo2(L.T0) + hi2(L.T0)) + (lo2(L.T1) + hi2(L.T1));
+}
+
+// The running maximum moved from L.m2 to m2n: rescale the sums.
+__device__ __forceinline__ void rescale(Lane &L, float m2n) {
+  if (L.zmax == -INFINITY) {
+    L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+    return;
+  }
+  const float d = L.m2 - m2n;  // <= 0
+  const float f = ex2_approx(d);
+  auto one = [&](uint64_t &S, uint64_t &T) {
+    float s0 = lo2(S), s1 = hi2(S), t0 = lo2(T), t1 = hi2(T);
+    t0 = fmaf(d, s0, t0) * f;
+    t1 = fmaf(d, s1, t1) * f;
+    S = pack2(s0 * f, s1 * f);
+    T = pack2(t0, t1);
+  };
+  one(L.S0, L.T0);
+  one(L.S1, L.T1);
+}
+
+// Element-wise evaluation of group g (n members, z[0..n) finite or -inf).
+__device__ __forceinline__ void gumbel_group_exact(const float *z, int n, uint32_t g, uint32_t h,
+                                                   float c, const Keys &K, Lane &L) {
+  const float X = exp1_draw(h);
+  const uint32_t J = below(fmix32(K.kb ^ g), (uint32_t)n);
+  const float base = X / (float)n;
+  for (int j = 0; j < n; ++j) {
+    float E = base;
+    if ((uint32_t)j != J) E += exp1_draw(fmix32(K.kc ^ (g * kGroup + (uint32_t)j)));
+    const float sc = fmaf(z[j], c, -log2f(E));
+    if (sc > L.b2) {
+      L.b2 = sc;
+      L.cand = (int32_t)(g * kGroup + j);
+    }
+  }
+}
+
+// Fast path for a full group of 8 finite logits.
+__device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c, const Keys &K,
+                                       Lane &L) {
+  const float vmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                           fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+  if (vmax > L.zmax) {
+    int j = 7;
+#pragma unroll
+    for (int jj = 6; jj >= 0; --jj)
+      if (z[jj] == vmax) j = jj;
+    const float m2n = vmax * c;
+    rescale(L, m2n);
+    L.zmax = vmax;
+    L.am = (int32_t)(g * kGroup + j);
+    L.m2 = m2n;
+  }
+  const uint64_t cc = pack2(c, c);
+  const uint64_t mm = pack2(-L.m2, -L.m2);
+  {
+    const uint64_t a0 = fma2(pack2(z[0], z[1]), cc, mm);
+    const uint64_t a1 = fma2(pack2(z[2], z[3]), cc, mm);
+    const uint64_t a2 = fma2(pack2(z[4], z[5]), cc, mm);
+    const uint64_t a3 = fma2(pack2(z[6], z[7]), cc, mm);
+    const uint64_t e0 = pack2(ex2_approx(lo2(a0)), ex2_approx(hi2(a0)));
+    const uint64_t e1 = pack2(ex2_approx(lo2(a1)), ex2_approx(hi2(a1)));
+    const uint64_t e2 = pack2(ex2_approx(lo2(a2)), ex2_approx(hi2(a2)));
+    const uint64_t e3 = pack2(ex2_approx(lo2(a3)), ex2_approx(hi2(a3)));
+    L.S0 = add2(L.S0, e0);
+    L.S1 = add2(L.S1, e1);
+    L.T0 = fma2(a0, e0, L.T0);
+    L.T1 = fma2(a1, e1, L.T1);
+    L.S0 = add2(L.S0, e2);
+    L.S1 = add2(L.S1, e3);
+    L.T0 = fma2(a2, e2, L.T0);
+    L.T1 = fma2(a3, e3, L.T1);
+  }
+  // Screen: the group can hold a score >= best only if its minimum
+  // exponential X/8 <= 2^(vmax*c - b2); X >= W = 1 - U, W from ~h.
+  const uint32_t h = fmix32(K.ka ^ g);
+  const float w = (float)(~h) * 2.3283064365386963e-10f;
+  const float thr = 8.0f * ex2_approx(fmaf(vmax, c, -L.b2));
+  if (w <= thr * 1.001f) gumbel_group_exact(z, 8, g, h, c, K, L);
+}
+
+// Careful path for any group (n <= 8 members, any values): flags NaN / +inf,
+// skips -inf, evaluates every finite member's Gumbel score exactly.
+__device__ void group_careful(const float *z, int n, uint32_t g, float c, const Keys &K, Lane &L,
+                              uint32_t &flags) {
+  float zz[8];
+  float vmax = -INFINITY;
+  int jm = -1;
+  for (int j = 0; j < n; ++j) {
+    float v = z[j];
+    if (isnan(v)) {
+      flags |= kPartNaN;
+      v = -INFINITY;
+    } else if (v == INFINITY) {
+      flags |= kPartPInf;
+      v = -INFINITY;
+    }
+    zz[j] = v;
+    if (v > vmax) {
+      vmax = v;
+      jm = j;
+    }
+  }
+  if (vmax == -INFINITY) return;  // nothing finite in this group
+  if (vmax > L.zmax) {
+    const float m2n = vmax * c;
+    rescale(L, m2n);
+    L.zmax = vmax;
+    L.am = (int32_t)(g * kGroup + jm);
+    L.m2 = m2n;
+  }
+  float s = 0.f, t = 0.f;
+  for (int j = 0; j < n; ++j) {
+    if (zz[j] == -INFINITY) continue;
+    const float a = fmaf(zz[j], c, -L.m2);
+    const float e = ex2_approx(a);
+    s += e;
+    t = fmaf(a, e, t);
+  }
+  L.S0 = add2(L.S0, pack2(s, 0.f));
+  L.T0 = add2(L.T0, pack2(t, 0.f));
+  gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, K, L);
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&z)[8]) {
+  z[0] = __uint_as_float(v.x << 16);
+  z[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  z[2] = __uint_as_float(v.y << 16);
+  z[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  z[4] = __uint_as_float(v.z << 16);
+  z[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  z[6] = __uint_as_float(v.w << 16);
+  z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+template <int DT>
+__device__ __forceinline__ float load_scalar(const void *row, int64_t v) {
+  if (DT == DG_BF16) {
+    const unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(row) + v);
+    return __uint_as_float((uint32_t)b << 16);
+  } else {
+    return __ldg(reinterpret_cast<const float *>(row) + v);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void load_group_scalar(const void *row, int64_t v, int n, float *z) {
+  for (int j = 0; j < n; ++j) z[j] = load_scalar<DT>(row, v + j);
+}
+
+// Merge the 32 lanes' records; every lane ends with the warp result.
+__device__ __forceinline__ void warp_merge(float c, float &zmax, int32_t &am, float &s, float &t,
+                                           float &b2, int32_t &cand) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float oz = __shfl_xor_sync(0xFFFFFFFFu, zmax, off);
+    const int32_t oam = __shfl_xor_sync(0xFFFFFFFFu, am, off);
+    const float os = __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    const float ot = __shfl_xor_sync(0xFFFFFFFFu, t, off);
+    const float ob = __shfl_xor_sync(0xFFFFFFFFu, b2, off);
+    const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cand, off);
+    // softmax sums, relative to fl(zmax * c) on each side
+    const float nz = fmaxf(zmax, oz);
+    if (nz != -INFINITY) {
+      const float M2 = nz * c;
+      float ns = 0.f, nt = 0.f;
+      if (s > 0.f) {
+        const float d = zmax * c - M2;
+        const float f = ex2_approx(d);
+        ns += s * f;
+        nt += fmaf(d, s, t) * f;
+      }
+      if (os > 0.f) {
+        const float d = oz * c - M2;
+        const float f = ex2_approx(d);
+        ns += os * f;
+        nt += fmaf(d, os, ot) * f;
+      }
+      s = ns;
+      t = nt;
+    }
+    if (oz > zmax || (oz == zmax && oam >= 0 && (am < 0 || oam < am))) {
+      zmax = oz;
+      am = oam;
+    }
+    if (ob > b2 || (ob == b2 && oc >= 0 && (cand < 0 || oc < cand))) {
+      b2 = ob;
+      cand = oc;
+    }
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kWarps * 32)
+    vocab_pass_kernel(const void *__restrict__ logits, int64_t ld, int32_t V, int32_t C,
+                      int64_t n_pos, int32_t chunk, int32_t n_chunks, uint64_t seed,
+                      const uint8_t *__restrict__ phase, const uint64_t *__restrict__ request_id,
+                      const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
+                      Partial *__restrict__ part, uint32_t *__restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t wg = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (wg >= n_pos * (int64_t)n_chunks) return;
+  const int64_t pos = wg / n_chunks;
+  const int32_t ch = (int32_t)(wg - pos * n_chunks);
+  const int64_t r = pos / C;
+  const int64_t i = pos - r * C;
+  if (phase[r] != DG_PHASE_DENOISE) return;
+  Partial *out = part + wg;
+
+  const float T = temperature[r];
+  if (!(T > 0.f) || !isfinite(T)) {
+    if (lane == 0) {
+      Partial P;
+      P.zmax = -INFINITY;
+      P.am = -1;
+      P.s = 0.f;
+      P.t = 0.f;
+      P.b2 = -INFINITY;
+      P.cand = -1;
+      P.flags = kPartBadT;
+      P.pad = 0;
+      *out = P;
+      if (ch == 0) atomicOr(status, (uint32_t)DG_DEV_BAD_TEMPERATURE);
+    }
+    return;
+  }
+  const float c = kLog2e / T;
+
+  const uint64_t pk = position_key(seed, request_id[r], rng_step[r], (uint64_t)i);
+  Keys K;
+  K.ka = (uint32_t)stream_key(pk, kTagGMin);
+  K.kb = (uint32_t)stream_key(pk, kTagGArg);
+  K.kc = (uint32_t)stream_key(pk, kTagGRest);
+
+  const int64_t v0 = (int64_t)ch * chunk;
+  const int64_t v1 = min((int64_t)V, v0 + chunk);
+  const size_t esz = (DT == DG_BF16) ? 2 : 4;
+  const char *row = reinterpret_cast<const char *>(logits) + (size_t)pos * (size_t)ld * esz;
+  const int32_t n_full = (int32_t)((v1 - v0) / kGroup);
+  const uint32_t g0 = (uint32_t)(v0 / kGroup);
+  const int tail_n = (int)((v1 - v0) - (int64_t)n_full * kGroup);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+
+  Lane L;
+  lane_init(L);
+  uint32_t flags = 0;
+
+  // ---- fast path over full groups
+  if (aligned) {
+    if (DT == DG_BF16) {
+      const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
+      int q = lane;
+      for (; q + 3 * 32 < n_full; q += 4 * 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = ld_stream(vrow + q + u * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float z[8];
+          unpack_bf16x8(v[u], z);
+          group8(z, g0 + (uint32_t)(q + u * 32), c, K, L);
+        }
+      }
+      for (; q < n_full; q += 32) {
+        float z[8];
+        unpack_bf16x8(ld_stream(vrow + q), z);
+        group8(z, g0 + (uint32_t)q, c, K, L);
+      }
+    } else {
+      const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
+      int q = lane;
+      for (; q + 1 * 32 < n_full; q += 2 * 32) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          v[2 * u] = ld_stream(vrow + 2 * (q + u * 32));
+          v[2 * u + 1] = ld_stream(vrow + 2 * (q + u * 32) + 1);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float z[8] = {__uint_as_float(v[2 * u].x),     __uint_as_float(v[2 * u].y),
+                        __uint_as_float(v[2 * u].z),     __uint_as_float(v[2 * u].w),
+                        __uint_as_float(v[2 * u + 1].x), __uint_as_float(v[2 * u + 1].y),
+                        __uint_as_float(v[2 * u + 1].z), __uint_as_float(v[2 * u + 1].w)};
+          group8(z, g0 + (uint32_t)(q + u * 32), c, K, L);
+        }
+      }
+      for (; q < n_full; q += 32) {
+        const uint4 a = ld_stream(vrow + 2 * q), b = ld_stream(vrow + 2 * q + 1);
+        float z[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                      __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
+                      __uint_as_float(b.z), __uint_as_float(b.w)};
+        group8(z, g0 + (uint32_t)q, c, K, L);
+      }
+    }
+  } else {
+    for (int q = lane; q < n_full; q += 32) {
+      float z[8];
+      load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
+      group8(z, g0 + (uint32_t)q, c, K, L);
+    }
+  }
+
+  float s, t;
+  sums(L, s, t);
+  const bool bad = !(isfinite(s) && isfinite(t));
+  if (__any_sync(0xFFFFFFFFu, bad)) {
+    // ---- careful path: redo the whole chunk
+    lane_init(L);
+    for (int q = lane; q < n_full; q += 32) {
+      float z[8];
+      load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
+      group_careful(z, 8, g0 + (uint32_t)q, c, K, L, flags);
+    }
+  }
+  if (tail_n > 0 && lane == (n_full & 31)) {
+    float z[8];
+    load_group_scalar<DT>(row, v0 + (int64_t)n_full * kGroup, tail_n, z);
+    group_careful(z, tail_n, g0 + (uint32_t)n_full, c, K, L, flags);
+  }
+  sums(L, s, t);
+
+  float zmax = L.zmax, b2 = L.b2;
+  int32_t am = L.am, cand = L.cand;
+  warp_merge(c, zmax, am, s, t, b2, cand);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, off);
+  if (lane == 0) {
+    Partial P;
+    P.zmax = zmax;
+    P.am = am;
+    P.s = s;
+    P.t = t;
+    P.b2 = b2;
+    P.cand = cand;
+    P.flags = flags;
+    P.pad = 0;
+    *out = P;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_state &st,
+                              Partial *part, int32_t chunk, int32_t n_chunks, cudaStream_t s) {
+  const int64_t n_pos = (int64_t)p.batch * p.canvas_len;
+  const int64_t warps = n_pos * n_chunks;
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  if (p.logits_dtype == DG_BF16) {
+    vocab_pass_kernel<DG_BF16><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
+        logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, st.phase,
+        st.request_id, st.temperature, st.rng_step, part, st.device_status);
+  } else {
+    vocab_pass_kernel<DG_F32><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
+        logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, st.phase,
+        st.request_id, st.temperature, st.rng_step, part, st.device_status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,169 @@
+/*
+ * dg.h -- C ABI of the GB300 (sm_103a) denoise-step sampler and
+ * self-conditioning feed of a uniform-state block-diffusion language model.
+ *
+ * One call of dg_denoise_step processes every request slot of a batch by its
+ * phase (prefill / denoise / commit / idle), as the single vectorised sample
+ * step of the vLLM blog "DiffusionGemma: the first dLLM natively supported in
+ * vLLM" (section "Putting it together: DiffusionGemmaModelState and
+ * DiffusionSampler") does.  dg_selfcond_embed computes the probability-weighted
+ * embedding softmax(z/T) . E of "DiffusionGemma Technical Report -- part 2/6",
+ * section 3.2, eq. 6.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *     never allocates, frees or synchronises, and keeps no pointer after a call
+ *     returns.  Scratch memory is the caller's workspace (dg_workspace_bytes).
+ *   - DG_OK means "enqueued on `stream`".  Launch failures are reported as
+ *     DG_ERR_CUDA (from cudaGetLastError).  Kernels never trap: conditions only
+ *     the device can see set bits in state->device_status (DG_DEV_*).
+ *   - Arguments are validated on the host before anything is enqueued; an
+ *     invalid call returns an error code and has no side effect.
+ *   - No host synchronisation: every call can be captured in a CUDA graph.
+ *   - Layouts: B = batch (request slots), C = canvas length, V = vocabulary.
+ *     logits are [B][C][ld] row-major, position (r, i) at row r*C + i, with
+ *     ld >= V elements between consecutive positions.  Per-position state
+ *     arrays are [B*C] at index r*C + i; per-request arrays are [B].
+ *   - Random numbers: a counter-based hash of (seed, request_id, rng_step,
+ *     position, tag) -- SplitMix64 key chain and MurmurHash3 fmix32 draws --
+ *     so a step is reproducible from its inputs alone.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+typedef enum {
+  DG_OK = 0,
+  DG_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, bad enum   */
+  DG_ERR_UNSUPPORTED = 2, /* device is not sm_103 / unsupported dtype combo    */
+  DG_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required   */
+  DG_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed            */
+} dg_status;
+
+/* Sticky bits OR-ed into state->device_status[0] by the kernels. */
+enum {
+  DG_DEV_NONFINITE_LOGITS = 1u, /* a denoise position held NaN / +inf or was all -inf */
+  DG_DEV_BAD_TEMPERATURE = 2u,  /* a denoise row had T <= 0 or non-finite             */
+  DG_DEV_BAD_TOKEN = 4u,        /* a committed token was outside [0, V)               */
+  DG_DEV_WAIT_TIMEOUT = 8u,     /* a bounded wait in the self-cond GEMM gave up       */
+  DG_DEV_BAD_PHASE = 16u        /* a phase value outside DG_PHASE_*                  */
+};
+
+/* Request phases (vLLM blog, "Putting it together": prefill, denoise, commit). */
+enum { DG_PHASE_PREFILL = 0, DG_PHASE_DENOISE = 1, DG_PHASE_COMMIT = 2, DG_PHASE_IDLE = 3 };
+
+/* Element types. */
+enum { DG_F32 = 0, DG_BF16 = 1 };
+
+/* Scalar parameters of a call (host memory, read during the call only). */
+typedef struct {
+  int32_t batch;          /* B >= 1 request slots                                */
+  int32_t canvas_len;     /* C, 1 <= C <= 1024 (the pages use 256)               */
+  int32_t vocab;          /* V, 2 <= V < 2^31                                    */
+  int32_t logits_dtype;   /* DG_F32 or DG_BF16                                   */
+  int64_t logits_ld;      /* elements between consecutive positions, >= V       */
+  uint64_t seed;          /* random-number seed of the whole run                 */
+  float entropy_budget;   /* nats, finite, >= 0 (acceptance budget)              */
+  float conf_threshold;   /* nats; converge when mean entropy < this (not NaN)   */
+  int32_t stable_k;       /* >= 1 consecutive equal argmax canvases              */
+  int32_t step_cap;       /* >= 1 maximum denoise steps per block                */
+} dg_params;
+
+/* Per-request state: device arrays, preallocated by the caller and updated in
+ * place (vLLM blog, "Putting it together": per-request state lives in
+ * preallocated GPU tensors).  Shapes [B] or [B*C].  All fields are required
+ * by dg_denoise_step; dg_init_canvas / dg_commit use the subset they touch. */
+typedef struct {
+  uint8_t *phase;              /* [B]   in/out DG_PHASE_*                            */
+  const uint64_t *request_id;  /* [B]   in   identity of the slot for the hash       */
+  const float *temperature;    /* [B]   in   T_r > 0 (caller anneals it if wanted)   */
+  uint64_t *rng_step;          /* [B]   in/out +1 per processed call, never reset    */
+  int32_t *step;               /* [B]   in/out denoise steps in the current block    */
+  int32_t *stable;             /* [B]   in/out consecutive equal argmax canvases     */
+  int32_t *canvas;             /* [B*C] out  next tokens (accepted cand or re-noise) */
+  int32_t *argmax_prev;        /* [B*C] in/out argmax canvas of the last step        */
+  int32_t *cand;               /* [B*C] out  Gumbel-max candidates                   */
+  int32_t *argmax;             /* [B*C] out  clean argmax of this step               */
+  uint8_t *accept;             /* [B*C] out  1 = accepted position                   */
+  float *m;                    /* [B*C] out  max_v z_v / T   (NaN if invalid)        */
+  float *s;                    /* [B*C] out  sum_v exp(z_v/T - m)                   */
+  float *entropy;              /* [B*C] out  H in nats      (NaN if invalid)        */
+  float *mean_entropy;         /* [B]   out  mean of H over the canvas              */
+  uint8_t *converged;          /* [B]   out  1 = converged this step                */
+  uint8_t *sc_valid;           /* [B]   out  1 = row feeds self-conditioning next    */
+  int32_t *num_sampled;        /* [B]   out  0 (prefill/denoise) or C (commit)       */
+  int32_t *num_rejected;       /* [B]   out  C (denoise) or 0                        */
+  int32_t *emitted;            /* [B*C] out  tokens emitted by commit rows           */
+  uint32_t *device_status;     /* [1]   in/out sticky DG_DEV_* bits                  */
+} dg_state;
+
+/* Bytes of caller workspace needed by dg_denoise_step and, if d > 0, by
+ * dg_selfcond_embed with embedding width d (one buffer serves both, as the
+ * calls are ordered on one stream).  Returns 0 if `p` is invalid.  Depends on
+ * the sizes in `p` and on d only. */
+size_t dg_workspace_bytes(const dg_params *p, int32_t d);
+
+/* Stand-alone canvas initialisation (the prefill case) of the rows r with
+ * row_mask[r] != 0 (device [B] uint8): canvas = uniform random tokens, counters
+ * reset, phase = DENOISE, rng_step += 1.  Technical Report section 3.2
+ * "Canvas initialization"; vLLM blog, prefill bullet.  Uses phase, request_id,
+ * rng_step, step, stable, canvas, converged, sc_valid, num_sampled,
+ * num_rejected. */
+int dg_init_canvas(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
+                   cudaStream_t stream);
+
+/* One sampler step over the whole batch, each row by its phase:
+ *   PREFILL -> as dg_init_canvas;  COMMIT -> as dg_commit;  IDLE -> untouched;
+ *   DENOISE -> per position: y = z/T, (m, s), entropy, clean argmax, Gumbel-max
+ *   candidate argmax(y + G); per canvas: entropy-bounded acceptance (positions
+ *   by ascending (H, i), accepted while the exclusive prefix sum of entropies
+ *   is <= budget, the first always), re-noise of rejected positions to uniform
+ *   tokens, convergence ((stable >= k and mean H < thr) or step >= cap) which
+ *   moves the row to COMMIT.
+ * Sources: "DiffusionGemma Explained" (ML@Berkeley), section "Sampling",
+ * steps 1-4; Technical Report section 3.3; vLLM blog sections "Entropy-bounded
+ * denoising" and "Putting it together".
+ * `logits`: device [B][C][logits_ld] of p->logits_dtype, aligned to its
+ * element size; only DENOISE rows are read.  `ws`: workspace of at least
+ * dg_workspace_bytes(p, 0) bytes.  Two kernel launches. */
+int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st,
+                    void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Self-conditioning feed, Technical Report section 3.2 eq. 6 (the p0 E inside
+ * FFW(p0 E)); "DiffusionGemma Explained", section "Self-conditioning":
+ *   out[r*C + i, :] = sum_v softmax(z_{r,i} / T_r)_v * E[v, :]
+ * for rows with sc_valid[r] = 1 and phase[r] = DENOISE and positions whose
+ * entropy is finite; every other output row is written as zeros (first
+ * decode step and encoder passes see zero self-conditioning: vLLM blog,
+ * "Self-conditioning").  Must follow dg_denoise_step on the same stream (it
+ * reads the m and s that step wrote) and use the same logits.
+ * `E`: device bf16 [V][ld_E], 16-byte aligned, ld_E >= d, ld_E*2 % 16 == 0.
+ * `d`: 16 <= d, d % 16 == 0.  `out`: device [B*C][d] of out_dtype (DG_F32 or
+ * DG_BF16).  `ws`: at least dg_workspace_bytes(p, d) bytes.  Products run on
+ * the tensor cores in bf16 with fp32 accumulation. */
+int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st,
+                      const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
+                      void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Stand-alone commit (the commit case) of the rows with row_mask[r] != 0:
+ * emitted = argmax_prev (the clean argmax canvas, vLLM blog "Entropy-bounded
+ * denoising"), num_sampled = C, num_rejected = 0, a fresh random canvas,
+ * counters reset, phase = DENOISE, rng_step += 1. */
+int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
+              cudaStream_t stream);
+
+/* Static description of a return code. */
+const char *dg_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DG_H */

@@ -30,7 +30,7 @@ readings table; the ones that change results are restated next to the code.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field
+from dataclasses import dataclass
 
 import numpy as np
 
@@ -256,14 +256,22 @@ def commit_row(p: Params, st: State, r: int):
     st.rng_step[r] = st.rng_step[r] + np.uint64(1)
 
 
-def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags):
-    """One denoise step of row r from its logits ``logits_row`` [C, V]."""
+def _vocab_job(args):
+    """One position's vocabulary pass (a picklable unit for a process pool)."""
+    z, T, seed, rid, rstep, i = args
+    ka, kb, kc = gumbel_keys(seed, rid, rstep, i)
+    return vocab_pass(z, T, ka, kb, kc)
+
+
+def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=map):
+    """One denoise step of row r from its logits ``logits_row`` [C, V].
+    ``mapper`` evaluates the independent per-position passes (``map`` or a
+    process pool's ``map``)."""
     C, V = p.canvas_len, p.vocab
     T = float(st.temperature[r])
+    jobs = [(logits_row[i], T, p.seed, st.request_id[r], st.rng_step[r], i) for i in range(C)]
     H = np.empty(C)
-    for i in range(C):
-        ka, kb, kc = gumbel_keys(p.seed, st.request_id[r], st.rng_step[r], i)
-        res = vocab_pass(logits_row[i], T, ka, kb, kc)
+    for i, res in enumerate(mapper(_vocab_job, jobs)):
         st.m[r, i] = res.m
         st.s[r, i] = res.s
         st.entropy[r, i] = res.entropy
@@ -294,7 +302,7 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags):
     st.rng_step[r] = st.rng_step[r] + np.uint64(1)
 
 
-def step(p: Params, st_in: State, logits, rows=None):
+def step(p: Params, st_in: State, logits, rows=None, mapper=map):
     """One sampler call over the whole batch: each row by its phase.
 
     ``logits`` is indexable as logits[r] -> [C, V] float64 (or convertible);
@@ -317,7 +325,7 @@ def step(p: Params, st_in: State, logits, rows=None):
         elif ph == PHASE_DENOISE:
             if rows is not None and r not in rows:
                 continue
-            denoise_row(p, st, r, np.asarray(logits[r], dtype=np.float64), flags)
+            denoise_row(p, st, r, np.asarray(logits[r], dtype=np.float64), flags, mapper)
     return st, flags
 
 

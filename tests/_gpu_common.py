@@ -1,0 +1,175 @@
+"""Helpers shared by the GPU parity tests: building device state, running the
+library through its binding, running the oracle on the GPU's prior state,
+and comparing under the stated tolerances and near-tie rules."""
+
+from __future__ import annotations
+
+import concurrent.futures as cf
+import multiprocessing as mp
+import os
+
+import numpy as np
+import torch
+
+import denoise_step_sampler_gb300 as dg
+from oracle import sampler as osam
+from oracle import selfcond as osc
+
+ENT_TOL = 1e-4       # entropy, absolute (nats)
+M_TOL = 1e-4         # m = max z / T, absolute
+S_RTOL = 1e-5        # s, relative
+SC_RTOL = 2e-2       # self-conditioning, relative (row norm and max-scaled elementwise)
+
+_POOL = None
+
+
+def pool():
+    """A spawn process pool for oracle positions (never forked after CUDA init)."""
+    global _POOL
+    if _POOL is None:
+        n = max(1, min(32, (os.cpu_count() or 2) - 1))
+        _POOL = cf.ProcessPoolExecutor(max_workers=n, mp_context=mp.get_context("spawn"))
+    return _POOL
+
+
+def pmap(fn, jobs):
+    jobs = list(jobs)
+    if len(jobs) < 8:
+        return list(map(fn, jobs))
+    return list(pool().map(fn, jobs, chunksize=max(1, len(jobs) // (4 * pool()._max_workers))))
+
+
+def make_state(p: dg.Params, phases, request_ids=None, temperatures=None, rng_step=None,
+               argmax_prev=None, device="cuda") -> dg.State:
+    st = dg.State(p.batch, p.canvas_len, device)
+    st.phase.copy_(torch.as_tensor(np.asarray(phases, np.uint8)))
+    if request_ids is not None:
+        st.request_id.copy_(torch.as_tensor(np.asarray(request_ids, np.uint64).view(np.int64)))
+    if temperatures is not None:
+        st.temperature.copy_(torch.as_tensor(np.asarray(temperatures, np.float32)))
+    if rng_step is not None:
+        st.rng_step.copy_(torch.as_tensor(np.asarray(rng_step, np.uint64).view(np.int64)))
+    if argmax_prev is not None:
+        st.argmax_prev.copy_(torch.as_tensor(np.asarray(argmax_prev, np.int32).reshape(-1)))
+    return st
+
+
+def oracle_params(p: dg.Params) -> osam.Params:
+    return osam.Params(batch=p.batch, canvas_len=p.canvas_len, vocab=p.vocab, seed=p.seed,
+                       entropy_budget=float(np.float32(p.entropy_budget)),
+                       conf_threshold=float(np.float32(p.conf_threshold)),
+                       stable_k=p.stable_k, step_cap=p.step_cap)
+
+
+def oracle_state(snap: dict, p: dg.Params) -> osam.State:
+    """The oracle's state built from a host snapshot of the device state."""
+    B, C = p.batch, p.canvas_len
+    st = osam.State(
+        phase=snap["phase"].copy(), request_id=snap["request_id"].copy(),
+        temperature=snap["temperature"].astype(np.float64),
+        rng_step=snap["rng_step"].copy(), step=snap["step"].copy(), stable=snap["stable"].copy(),
+        canvas=snap["canvas"].reshape(B, C).copy(), argmax_prev=snap["argmax_prev"].reshape(B, C).copy())
+    osam._ensure_outputs(st, B, C)
+    st.emitted = snap["emitted"].reshape(B, C).copy()
+    return st
+
+
+def run_oracle_step(p: dg.Params, snap_before: dict, logits_host, rows=None):
+    """Oracle step from the GPU's prior state; ``logits_host`` indexable [B][C, ld]."""
+    op = oracle_params(p)
+    st0 = oracle_state(snap_before, p)
+
+    class _Rows:
+        def __getitem__(self, r):
+            return np.asarray(logits_host[r])[:, :p.vocab].astype(np.float64)
+
+    return osam.step(op, st0, _Rows(), rows=rows, mapper=pmap)
+
+
+def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags: osam.Flags,
+                 rows=None, positions=None):
+    """Assert the GPU's post-step state equals the oracle's, up to tolerances
+    and the oracle's near-tie flags.  Returns counts of flagged decisions."""
+    B, C = p.batch, p.canvas_len
+    rows = range(B) if rows is None else rows
+    n_flag = {"cand": 0, "accept": 0, "converged": 0}
+    for r in rows:
+        ph = int(before["phase"][r])
+        sl = slice(r * C, (r + 1) * C)
+        g = {k: after[k] for k in after}
+        if ph == dg.DG_PHASE_IDLE:
+            for k in ("canvas", "argmax_prev", "emitted"):
+                assert np.array_equal(g[k][sl], before[k][sl]), (r, k)
+            assert g["rng_step"][r] == before["rng_step"][r]
+            continue
+        assert g["rng_step"][r] == ost.rng_step[r], r
+        if ph in (dg.DG_PHASE_PREFILL, dg.DG_PHASE_COMMIT):
+            assert np.array_equal(g["canvas"][sl], ost.canvas[r]), (r, "canvas")
+            for k in ("step", "stable", "num_sampled", "num_rejected", "sc_valid", "phase"):
+                assert g[k][r] == getattr(ost, k)[r], (r, k)
+            if ph == dg.DG_PHASE_COMMIT:
+                assert np.array_equal(g["emitted"][sl], ost.emitted[r]), (r, "emitted")
+            continue
+        # DENOISE
+        valid = ~np.isnan(ost.entropy[r])
+        assert np.array_equal(np.isnan(g["entropy"][sl]), ~valid), (r, "validity")
+        v = valid
+        assert np.all(np.abs(g["entropy"][sl][v] - ost.entropy[r][v]) <= ENT_TOL), (r, "entropy",
+               np.max(np.abs(g["entropy"][sl][v] - ost.entropy[r][v])))
+        assert np.all(np.abs(g["m"][sl][v] - ost.m[r][v]) <= M_TOL), (r, "m")
+        assert np.all(np.abs(g["s"][sl][v] / ost.s[r][v] - 1.0) <= S_RTOL), (r, "s")
+        assert np.array_equal(g["argmax"][sl], ost.argmax[r]), (r, "argmax")
+        assert np.array_equal(g["argmax_prev"][sl], ost.argmax_prev[r]), (r, "argmax_prev")
+        fc = flags.cand[r]
+        n_flag["cand"] += int(fc.sum())
+        assert np.array_equal(g["cand"][sl][~fc], ost.cand[r][~fc]), (r, "cand")
+        if flags.accept[r]:
+            n_flag["accept"] += 1
+        else:
+            assert np.array_equal(g["accept"][sl], ost.accept[r]), (r, "accept")
+            ok = ~(fc & (ost.accept[r] == 1))
+            assert np.array_equal(g["canvas"][sl][ok], ost.canvas[r][ok]), (r, "canvas")
+        mh = ost.mean_entropy[r]
+        if np.isnan(mh):
+            assert np.isnan(g["mean_entropy"][r])
+        else:
+            assert abs(g["mean_entropy"][r] - mh) <= ENT_TOL, (r, "mean_entropy")
+        for k in ("step", "stable", "num_sampled", "num_rejected"):
+            assert g[k][r] == getattr(ost, k)[r], (r, k)
+        if flags.converged[r]:
+            n_flag["converged"] += 1
+        else:
+            for k in ("converged", "sc_valid", "phase"):
+                assert g[k][r] == getattr(ost, k)[r], (r, k)
+    return n_flag
+
+
+def denoise_and_compare(p: dg.Params, st: dg.State, logits: torch.Tensor, rows=None):
+    """Run one library step and the oracle from the same prior state."""
+    before = st.snapshot()
+    ws = torch.empty(dg.dg_workspace_bytes(p, 0), dtype=torch.uint8, device=logits.device)
+    dg.dg_denoise_step(p, logits, st, ws)
+    torch.cuda.synchronize()
+    after = st.snapshot()
+    ld = p.vocab if p.logits_ld is None else p.logits_ld
+    host = logits.view(p.batch, p.canvas_len, ld).float().cpu().numpy()
+    ost, flags = run_oracle_step(p, before, host, rows=rows)
+    n = compare_step(p, before, after, ost, flags, rows=rows)
+    return before, after, ost, flags, n
+
+
+def selfcond_check(got: np.ndarray, ref: np.ndarray):
+    """Per row: ||d||/||ref|| <= 2e-2 and max|d| <= 2e-2 * max|ref|; zero rows exact."""
+    for q in range(ref.shape[0]):
+        rr, gg = ref[q], got[q]
+        nr = np.linalg.norm(rr)
+        if nr == 0.0:
+            assert np.all(gg == 0.0), q
+            continue
+        d = gg - rr
+        assert np.linalg.norm(d) <= SC_RTOL * nr, (q, np.linalg.norm(d) / nr)
+        assert np.max(np.abs(d)) <= SC_RTOL * np.max(np.abs(rr)), q
+
+
+def oracle_selfcond_rows(logits_rows: np.ndarray, T: float, E: np.ndarray) -> np.ndarray:
+    return osc.selfcond_rows(logits_rows, T, E)

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every entry point include/dg.h declares, and rejects invalid arguments on the
+host before anything reaches a GPU.  No kernel is launched here."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+import torch
+
+import denoise_step_sampler_gb300 as dg
+from denoise_step_sampler_gb300 import build as dgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dg.h")
+
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(
+    "/usr/local/cuda/bin/nvcc"), reason="nvcc not available")
+
+
+@pytest.fixture(scope="module")
+def L():
+    dgbuild.build()
+    return dg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dg_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) >= {"dg_init_canvas", "dg_denoise_step", "dg_selfcond_embed", "dg_commit",
+                          "dg_workspace_bytes", "dg_status_string"}
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(5):
+        assert dg.dg_status_string(code)
+    assert dg.dg_status_string(99) == "unknown status"
+
+
+def _params(**kw):
+    base = dict(batch=2, canvas_len=256, vocab=1000, logits_dtype=dg.DG_F32, seed=1,
+                entropy_budget=10.0, conf_threshold=0.3, stable_k=3, step_cap=8)
+    base.update(kw)
+    return dg.Params(**base)
+
+
+def test_workspace_query(L):
+    p = _params()
+    a = dg.dg_workspace_bytes(p, 0)
+    assert a > 0 and a % 256 == 0
+    assert dg.dg_workspace_bytes(p, 64) >= a
+    assert dg.dg_workspace_bytes(_params(batch=8), 0) >= a
+    for bad in (dict(batch=0), dict(canvas_len=0), dict(canvas_len=2048), dict(vocab=1),
+                dict(logits_dtype=7), dict(logits_ld=999), dict(entropy_budget=-1.0),
+                dict(entropy_budget=float("inf")), dict(conf_threshold=float("nan")),
+                dict(stable_k=0), dict(step_cap=0)):
+        assert dg.dg_workspace_bytes(_params(**bad), 0) == 0, bad
+    assert L.dg_workspace_bytes(None, 0) == 0
+
+
+def _fake_state():
+    # distinct non-null fake device addresses; validation must fail before use
+    st = dg._CState(*[0x1000 + 0x100 * i for i in range(len(dg._STATE_FIELDS))])
+    return st
+
+
+def test_invalid_arguments_are_rejected_on_host(L):
+    p = _params().c()
+    st = _fake_state()
+    fake = ctypes.c_void_p(0x7000)
+    ws = ctypes.c_void_p(0x9000)
+    need = L.dg_workspace_bytes(ctypes.byref(p), 0)
+    E = ctypes.c_void_p(0xA000)
+    out = ctypes.c_void_p(0xB000)
+    # null params / state / logits
+    assert L.dg_denoise_step(None, fake, ctypes.byref(st), ws, need, None) == dg.DG_ERR_INVALID_ARG
+    assert L.dg_denoise_step(ctypes.byref(p), fake, None, ws, need, None) == dg.DG_ERR_INVALID_ARG
+    assert L.dg_denoise_step(ctypes.byref(p), None, ctypes.byref(st), ws, need, None) == dg.DG_ERR_INVALID_ARG
+    # a null field in the state
+    st2 = _fake_state()
+    st2.entropy = None
+    assert L.dg_denoise_step(ctypes.byref(p), fake, ctypes.byref(st2), ws, need, None) == dg.DG_ERR_INVALID_ARG
+    # misaligned logits
+    assert L.dg_denoise_step(ctypes.byref(p), ctypes.c_void_p(0x7001), ctypes.byref(st), ws, need,
+                             None) == dg.DG_ERR_INVALID_ARG
+    # workspace too small or missing
+    assert L.dg_denoise_step(ctypes.byref(p), fake, ctypes.byref(st), ws, need - 1, None) == dg.DG_ERR_WORKSPACE
+    assert L.dg_denoise_step(ctypes.byref(p), fake, ctypes.byref(st), None, need, None) == dg.DG_ERR_WORKSPACE
+    # self-cond: bad widths, strides, dtypes, alignment
+    for d, ldE, odt in ((0, 64, 0), (24, 24, 0), (64, 60, 0), (64, 68, 0), (64, 64, 5)):
+        assert L.dg_selfcond_embed(ctypes.byref(p), fake, ctypes.byref(st), E, d, ldE, out, odt,
+                                   ws, 1 << 30, None) == dg.DG_ERR_INVALID_ARG, (d, ldE, odt)
+    assert L.dg_selfcond_embed(ctypes.byref(p), fake, ctypes.byref(st), ctypes.c_void_p(0xA008),
+                               64, 64, out, 0, ws, 1 << 30, None) == dg.DG_ERR_INVALID_ARG
+    # init / commit need a row mask
+    assert L.dg_init_canvas(ctypes.byref(p), ctypes.byref(st), None, None) == dg.DG_ERR_INVALID_ARG
+    assert L.dg_commit(ctypes.byref(p), ctypes.byref(st), None, None) == dg.DG_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful without a GPU")
+def test_valid_call_without_gpu_reports_cuda_error(L):
+    p = _params().c()
+    st = _fake_state()
+    need = L.dg_workspace_bytes(ctypes.byref(p), 0)
+    rc = L.dg_denoise_step(ctypes.byref(p), ctypes.c_void_p(0x7000), ctypes.byref(st),
+                           ctypes.c_void_p(0x9000), need, None)
+    assert rc in (dg.DG_ERR_CUDA, dg.DG_ERR_UNSUPPORTED)
+
+
+def test_binding_checks_shapes_before_calling():
+    p = _params()
+    with pytest.raises(ValueError):
+        dg.dg_denoise_step(p, torch.zeros(10), dg.State.__new__(dg.State), torch.zeros(1))

@@ -1,0 +1,94 @@
+"""GPU parity of dg_selfcond_embed (the tcgen05 p.E contraction) against the
+fp64 oracle: ragged M / N / K tiles, split-K and single-pass plans, both
+logit dtypes, fp32 and bf16 outputs, padded E rows, rows that do not feed the
+next step, and the one-hot case that must return embedding rows exactly."""
+
+import numpy as np
+import pytest
+import torch
+
+import denoise_step_sampler_gb300 as dg
+from denoise_step_sampler_gb300 import synthetic as syn
+
+from _gpu_common import make_state, oracle_selfcond_rows, selfcond_check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from denoise_step_sampler_gb300 import build
+    build.build()
+    dg.lib()
+
+
+def _run(p, st, logits, E, out_dtype=torch.float32):
+    d = E.shape[1]
+    ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device="cuda")
+    dg.dg_denoise_step(p, logits, st, ws)
+    out = torch.full((p.batch * p.canvas_len, d), float("nan"), dtype=out_dtype, device="cuda")
+    dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+    torch.cuda.synchronize()
+    return out
+
+
+CASES = [
+    # (B, C, V, dtype, ld, d, ldE, out)
+    (2, 64, 64, dg.DG_F32, None, 16, 16, torch.float32),
+    (2, 128, 1000, dg.DG_BF16, None, 64, 64, torch.float32),
+    (1, 200, 1003, dg.DG_F32, 1003, 272, 288, torch.float32),
+    (3, 64, 4096, dg.DG_BF16, None, 128, 128, torch.bfloat16),
+    (1, 256, 20000, dg.DG_BF16, None, 512, 512, torch.float32),
+    (4, 256, 3000, dg.DG_BF16, None, 768, 768, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}C{c[1]}V{c[2]}d{c[5]}" for c in CASES])
+def test_selfcond_matches_oracle(case):
+    B, C, V, dt, ld, d, ldE, odt = case
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dt, logits_ld=ld, seed=21,
+                  entropy_budget=50.0, conf_threshold=-1.0, stable_k=3, step_cap=1000)
+    temps = np.linspace(0.7, 1.3, B)
+    st = make_state(p, [dg.DG_PHASE_DENOISE] * B, temperatures=temps)
+    tdt = torch.bfloat16 if dt == dg.DG_BF16 else torch.float32
+    logits = syn.boosted_logits(B * C, V, seed=V + d, dtype=tdt, device="cuda", ld=ld).reshape(-1)
+    Efull = syn.embedding(V, ldE, seed=d, device="cuda")
+    E = Efull[:, :d]
+    out = _run(p, st, logits, E, odt)
+    got = out.float().cpu().numpy()
+    Eh = E.float().cpu().numpy().astype(np.float64)
+    ldv = V if ld is None else ld
+    zh = logits.view(B, C, ldv)[:, :, :V].float().cpu().numpy()
+    tol_scale = 1.0 if odt == torch.float32 else 1.0
+    for r in range(B):
+        ref = oracle_selfcond_rows(zh[r], float(np.float32(temps[r])), Eh)
+        selfcond_check(got[r * C:(r + 1) * C], ref * tol_scale)
+
+
+def test_selfcond_one_hot_returns_embedding_rows_exactly():
+    B, C, V, d = 1, 128, 777, 64
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_F32, seed=2,
+                  entropy_budget=50.0, conf_threshold=-1.0, step_cap=100)
+    st = make_state(p, [dg.DG_PHASE_DENOISE], temperatures=[0.8])
+    tok = torch.randint(0, V, (C,), device="cuda")
+    logits = torch.full((C, V), float("-inf"), device="cuda")
+    logits[torch.arange(C, device="cuda"), tok] = torch.randn(C, device="cuda")
+    E = syn.embedding(V, d, seed=5, device="cuda")
+    out = _run(p, st, logits.reshape(-1), E)
+    assert torch.equal(out, E[tok].float())
+
+
+def test_rows_that_do_not_feed_are_zero():
+    B, C, V, d = 4, 64, 500, 32
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=4,
+                  entropy_budget=50.0, conf_threshold=-1.0, stable_k=1, step_cap=2)
+    st = make_state(p, [dg.DG_PHASE_DENOISE, dg.DG_PHASE_PREFILL, dg.DG_PHASE_IDLE,
+                        dg.DG_PHASE_DENOISE], temperatures=[1, 1, 1, 1])
+    st.step[3] = 1  # reaches the cap: converges, does not feed
+    logits = syn.boosted_logits(B * C, V, seed=1, device="cuda").reshape(-1)
+    E = syn.embedding(V, d, seed=6, device="cuda")
+    out = _run(p, st, logits, E).view(B, C, d)
+    assert torch.count_nonzero(out[1:]).item() == 0
+    assert torch.count_nonzero(out[0]).item() > 0
+    snap = st.snapshot()
+    assert snap["sc_valid"].tolist() == [1, 0, 0, 0]
