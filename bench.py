@@ -326,17 +326,18 @@ def run_ours(args, rank, world, dev):
 
 
 def _selfcond_splits(rows, V, d):
-    # mirrors the library's plan only to count launches (it does not affect timing)
-    BM, BN, BK, SMS = 128, 256, 64, 152
+    # mirrors the library's split plan only to count launches (no effect on timing)
+    BM, BN, BK, SMS = 128, 512, 32, 152
     m, n, k = -(-rows // BM), -(-d // BN), -(-V // BK)
+    halves = -(-d // 256)
     tiles = m * n
     best, best_eff = 1, 0.0
-    for sp in range(1, 33):
-        if sp > 1 and k // sp < 8:
+    for sp in range(1, 65):
+        if sp > 1 and k // sp < 16:
             break
         ctas = tiles * sp
         waves = -(-ctas // SMS)
-        eff = ctas / (waves * SMS)
+        eff = m * halves * 0.5 * sp / (waves * SMS)
         if eff > best_eff + 0.05:
             best, best_eff = sp, eff
     kbps = -(-k // best)

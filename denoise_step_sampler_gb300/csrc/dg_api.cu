@@ -150,6 +150,12 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
   return DG_OK;
 }
 
+int dg_debug_wait_record(uint32_t out[4]) {
+  if (!out) return DG_ERR_INVALID_ARG;
+  if (dg_selfcond_wait_record(out) != cudaSuccess) return DG_ERR_CUDA;
+  return DG_OK;
+}
+
 const char *dg_status_string(int code) {
   switch (code) {
     case DG_OK:

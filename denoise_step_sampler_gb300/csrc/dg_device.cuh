@@ -55,8 +55,10 @@ __device__ __forceinline__ uint32_t below(uint32_t h, uint32_t n) {
 // complement so that small values keep their relative precision.
 __device__ __forceinline__ float exp1_draw(uint32_t h) {
   if (h < 0x80000000u) {
+    // u <= 1/2: -ln u >= ln 2, so the absolute error of the fast logarithm
+    // (about 2^-22 |ln u|) stays a relative error of about 2^-22.
     const float u = fmaf((float)h, 2.3283064365386963e-10f, 1.1641532182693481e-10f);
-    return -logf(u);
+    return -__logf(u);
   }
   const float w = fmaf((float)(~h), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
   return -log1pf(-w);

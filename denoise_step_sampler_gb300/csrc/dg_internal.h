@@ -36,4 +36,8 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                             void *ws, const SelfcondPlan &plan, cudaStream_t s);
 
+// Copies the self-cond GEMM's first wait-timeout record to host memory
+// (synchronous; diagnostics only).
+cudaError_t dg_selfcond_wait_record(uint32_t out[4]);
+
 }  // namespace dg

@@ -2,18 +2,24 @@
 // Blackwell tensor cores (Technical Report section 3.2, eq. 6: the p0 E inside
 // FFW(p0 E)).
 //
-// The probabilities are never stored: producer warps rebuild each 128 x 64
-// bf16 tile of p from the logits and the per-position (m, s) written by the
-// sampler step, p = 2^(z*log2(e)/T - (m*log2(e) + log2 s)), and write it into
-// shared memory in the 128-byte-swizzled K-major layout the MMA reads.  The
-// E tile (64 vocabulary rows x 256 embedding columns, bf16, N-major) arrives
-// by TMA.  One thread issues tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 ->
-// fp32) into a TMEM accumulator; the epilogue reads it back with tcgen05.ld.
+// The probabilities are never stored: each 128 x 32 tile of bf16 logits
+// arrives by TMA in the 64-byte-swizzled K-major layout the MMA reads, and
+// eight producer warps turn it into p in place,
+// p = 2^(z*log2(e)/T - (m*log2(e) + log2 s)), from the per-position (m, s)
+// the sampler step wrote (fp32 or unaligned logits are loaded by the producers
+// instead).  The E tile (32 vocabulary rows x 512 embedding columns, bf16,
+// N-major, 128-byte swizzle) arrives by TMA.  One thread issues two
+// tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) per 16 vocabulary
+// rows into a 512-column TMEM accumulator, so every exponential feeds 512
+// columns of MMA work; the epilogue reads TMEM back with tcgen05.ld.
 // Small batches split the vocabulary (K) across CTAs and reduce the fp32
 // partial sums in a second kernel.  Every wait is bounded: a wait that gives up
 // sets DG_DEV_WAIT_TIMEOUT, the CTA drains what it issued and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <cstring>
+#include <algorithm>
 
 #include "dg_device.cuh"
 #include "dg_internal.h"
@@ -22,21 +28,25 @@ namespace dg {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int NST = 4;
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 producers/epilogue
-constexpr int kProdWarps = 4;
-constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr int BN = 512;  // two N=256 MMAs per k-step
+constexpr int BK = 32;   // one 64-byte swizzle row of bf16
+constexpr int NST = 5;
+constexpr int kProdWarps = 8;
+constexpr int kThreads = 64 + 32 * kProdWarps;  // warp 0 TMA, warp 1 MMA, 8 producer/epilogue
+constexpr uint32_t kABytes = BM * BK * 2;  // 8 KB
+constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 32 rows x 128 B
 constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
 constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + 2048 + 1024;
 constexpr int kAssumedSMs = 152;
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
+#ifndef DG_WAIT_NS
+#define DG_WAIT_NS 2000000000ull
+#endif
+constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
 
 struct Shared {
-  uint64_t full_a[NST];
-  uint64_t full_b[NST];
-  uint64_t empty[NST];
+  uint64_t full[NST];     // TMA bytes of the stage landed
+  uint64_t a_ready[NST];  // producers wrote p into the A tile
+  uint64_t empty[NST];    // the MMAs reading the stage completed
   uint64_t tmem_full;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -76,15 +86,34 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+}  // namespace
+
+// First wait that gave up since load (diagnostics): {set, block, where, parity}.
+// where = role << 28 | barrier << 24 | stage << 16 | k-iteration (low 16 bits);
+// roles 0 TMA, 1 MMA, 2 producer, 3 epilogue; barriers 0 full, 1 a_ready,
+// 2 empty, 3 tmem_full.
+__device__ uint32_t g_wait_record[4];
+
+namespace {
+
+__device__ __forceinline__ uint32_t where_code(uint32_t role, uint32_t bar, int stage, int iter) {
+  return (role << 28) | (bar << 24) | ((uint32_t)stage << 16) | ((uint32_t)iter & 0xFFFFu);
+}
+
 // Bounded wait; false if it gave up or another role aborted.
 __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Shared *sh,
-                                       uint32_t *status) {
+                                       uint32_t *status, uint32_t where) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try(b, parity)) {
     if (*(volatile int32_t *)&sh->abort_flag) return false;
     if (globaltimer() - t0 > kWaitNs) {
       *(volatile int32_t *)&sh->abort_flag = 1;
       atomicOr(status, (uint32_t)DG_DEV_WAIT_TIMEOUT);
+      if (atomicCAS(&g_wait_record[0], 0u, 1u) == 0u) {
+        g_wait_record[1] = blockIdx.x;
+        g_wait_record[2] = where;
+        g_wait_record[3] = parity;
+      }
       return false;
     }
   }
@@ -107,20 +136,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor (tcgen05 format); swz: 2 = 128-byte,
+// 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t swz) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  d |= (uint64_t)swz << 61;
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B N-major, M=128, N=BN.
+// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B N-major, M=128, N=256.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+                            ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
@@ -168,7 +199,8 @@ struct GemmArgs {
   int64_t ld;
   int32_t V, C, d, dtype;
   int64_t rows;  // B*C
-  int32_t n_tiles, splits, k_blocks, kb_per_split;
+  int32_t m_tiles, n_tiles, splits, k_blocks, kb_per_split;
+  int32_t tma_a;  // 1: bf16 logits tiles arrive by TMA; 0: producers load them
   const uint8_t *phase;
   const uint8_t *sc_valid;
   const float *temperature;
@@ -191,69 +223,103 @@ __device__ __forceinline__ bool row_feeds(const GemmArgs &a, int64_t q, float &c
   return true;
 }
 
-// Load 8 consecutive logits of row `row` starting at column k (columns >= V
-// read as -inf, i.e. probability 0).
-__device__ __forceinline__ void load8(const GemmArgs &a, const char *rowp, bool vec_ok, int64_t k,
-                                      float (&z)[8]) {
-  if (vec_ok && k + 8 <= a.V) {
-    if (a.dtype == DG_BF16) {
+// 8 consecutive logits of one row from global memory, as raw words: bf16
+// pairs (w[0..3]) or fp32 (w[0..7]); columns >= V come back as -inf.
+struct Raw8 {
+  uint32_t w[8];
+};
+__device__ __forceinline__ Raw8 load_raw8(const GemmArgs &a, const char *rowp, int64_t k) {
+  Raw8 r;
+  const bool vec_ok = ((reinterpret_cast<uintptr_t>(rowp) & 15u) == 0) && (k + 8 <= a.V);
+  if (a.dtype == DG_BF16) {
+    if (vec_ok) {
       const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rowp + k * 2));
-      z[0] = __uint_as_float(v.x << 16);
-      z[1] = __uint_as_float(v.x & 0xFFFF0000u);
-      z[2] = __uint_as_float(v.y << 16);
-      z[3] = __uint_as_float(v.y & 0xFFFF0000u);
-      z[4] = __uint_as_float(v.z << 16);
-      z[5] = __uint_as_float(v.z & 0xFFFF0000u);
-      z[6] = __uint_as_float(v.w << 16);
-      z[7] = __uint_as_float(v.w & 0xFFFF0000u);
+      r.w[0] = v.x; r.w[1] = v.y; r.w[2] = v.z; r.w[3] = v.w;
     } else {
-      const float4 u = __ldg(reinterpret_cast<const float4 *>(rowp + k * 4));
-      const float4 w = __ldg(reinterpret_cast<const float4 *>(rowp + k * 4 + 16));
-      z[0] = u.x; z[1] = u.y; z[2] = u.z; z[3] = u.w;
-      z[4] = w.x; z[5] = w.y; z[6] = w.z; z[7] = w.w;
-    }
-    return;
-  }
+      const unsigned short *b = reinterpret_cast<const unsigned short *>(rowp);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int64_t kk = k + j;
-    if (kk < a.V) {
-      if (a.dtype == DG_BF16)
-        z[j] = __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(rowp) + kk)
-                               << 16);
-      else
-        z[j] = __ldg(reinterpret_cast<const float *>(rowp) + kk);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = (k + 2 * j < a.V) ? (uint32_t)__ldg(b + k + 2 * j) : 0xFF80u;
+        const uint32_t hi = (k + 2 * j + 1 < a.V) ? (uint32_t)__ldg(b + k + 2 * j + 1) : 0xFF80u;
+        r.w[j] = lo | (hi << 16);
+      }
+    }
+  } else {
+    if (vec_ok) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4 *>(rowp + k * 4));
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(rowp + k * 4 + 16));
+      r.w[0] = u.x; r.w[1] = u.y; r.w[2] = u.z; r.w[3] = u.w;
+      r.w[4] = v.x; r.w[5] = v.y; r.w[6] = v.z; r.w[7] = v.w;
     } else {
-      z[j] = -INFINITY;
+      const uint32_t *f = reinterpret_cast<const uint32_t *>(rowp);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r.w[j] = (k + j < a.V) ? __ldg(f + k + j) : 0xFF800000u;
     }
   }
+  return r;
+}
+
+// p for 8 logits (bf16 pairs or fp32), packed to bf16; columns at or past V
+// (given by `valid`, a count from the chunk start) become exactly 0.
+__device__ __forceinline__ uint4 p_from_bf16(const uint32_t (&w)[4], float c, float l2,
+                                             int valid) {
+  float z[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    z[2 * j] = __uint_as_float(w[j] << 16);
+    z[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+  float p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) p[j] = (j < valid) ? ex2_approx(fmaf(z[j], c, -l2)) : 0.f;
+  return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                    pack_bf16x2(p[6], p[7]));
+}
+__device__ __forceinline__ uint4 p_from_f32(const uint32_t (&w)[8], float c, float l2,
+                                            int valid) {
+  float p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    p[j] = (j < valid) ? ex2_approx(fmaf(__uint_as_float(w[j]), c, -l2)) : 0.f;
+  return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                    pack_bf16x2(p[6], p[7]));
+}
+
+// Byte offset of 16-byte chunk `ch` (0..3) of row `r` in a 64-byte-swizzled
+// K-major tile (8-row atoms of 512 bytes).
+__device__ __forceinline__ uint32_t a_off(int r, int ch) {
+  return (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e, GemmArgs a) {
+    selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
+                         const __grid_constant__ CUtensorMap tmap_z, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t *sA = smem;                    // NST x 16 KB
-  uint8_t *sB = smem + NST * kABytes;    // NST x 32 KB
+  uint8_t *sB = smem;                   // NST x 32 KB (1024-aligned)
+  uint8_t *sA = smem + NST * kBBytes;   // NST x 8 KB
   Shared *sh = reinterpret_cast<Shared *>(smem + NST * (kABytes + kBBytes));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x;
   const int n_t = tile % a.n_tiles;
   const int rest = tile / a.n_tiles;
-  const int m_t = rest % (int)((a.rows + BM - 1) / BM);
-  const int split = rest / (int)((a.rows + BM - 1) / BM);
+  const int m_t = rest % a.m_tiles;
+  const int split = rest / a.m_tiles;
   const int64_t row0 = (int64_t)m_t * BM;
   const int n0 = n_t * BN;
   const int kb0 = split * a.kb_per_split;
   const int kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
   const int nkb = max(0, kb1 - kb0);
+  const int n_half = (n0 + 256 < a.d) ? 2 : 1;                    // MMAs per k-step
+  const int n_box = min(BN / 64, (a.d - n0 + 63) / 64);           // E boxes per stage
+  const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes + (a.tma_a ? kABytes : 0u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&sh->full_a[s], kProdWarps);
-      mbar_init(&sh->full_b[s], 1);
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->a_ready[s], kProdWarps);
       mbar_init(&sh->empty[s], 1);
     }
     mbar_init(&sh->tmem_full, 1);
@@ -262,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->any_valid = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp >= 2) {
-    const int t = threadIdx.x - 64;  // 0..127
+  if (warp >= 2 && threadIdx.x - 64 < BM) {
+    const int t = threadIdx.x - 64;
     float c = 0.f, l2 = 0.f;
     const bool ok = row_feeds(a, row0 + t, c, l2);
     sh->row_c[t] = c;
@@ -285,24 +351,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (run) {
     if (warp == 0) {
-      // ------------------------------------------------ TMA producer (E tiles)
+      // ------------------------------------------------ TMA producer
       if (lane == 0) {
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
           const uint32_t use = (uint32_t)(i / NST);
-          if (i >= NST && !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status)) break;
-          mbar_expect_tx(&sh->full_b[s], kBBytes);
-          uint8_t *dst = sB + s * kBBytes;
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j)
-            tma_load_2d(dst + j * (BK * 128), &tmap_e, &sh->full_b[s], n0 + j * 64,
-                        (kb0 + i) * BK);
+          if (i >= NST &&
+              !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
+            break;
+          mbar_expect_tx(&sh->full[s], stage_tx);
+          const int32_t kv = (kb0 + i) * BK;
+          uint8_t *dstB = sB + s * kBBytes;
+          for (int j = 0; j < n_box; ++j)
+            tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
+          if (a.tma_a) tma_load_2d(sA + s * kABytes, &tmap_z, &sh->full[s], kv, (int32_t)row0);
           issued = i + 1;
         }
-        // drain: every issued copy must land before the CTA may exit
+        // every issued copy must land before the CTA may exit
         for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(&sh->full_b[i % NST], (uint32_t)(i / NST) & 1u);
+          mbar_drain(&sh->full[i % NST], (uint32_t)(i / NST) & 1u);
       }
     } else if (warp == 1) {
       // ------------------------------------------------ MMA issuer
@@ -310,16 +378,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
           const uint32_t par = (uint32_t)(i / NST) & 1u;
-          if (!mbar_wait(&sh->full_b[s], par, sh, a.status)) break;
-          if (!mbar_wait(&sh->full_a[s], par, sh, a.status)) break;
+          if (!mbar_wait(&sh->full[s], par, sh, a.status, where_code(1, 0, s, i))) break;
+          if (!mbar_wait(&sh->a_ready[s], par, sh, a.status, where_code(1, 1, s, i))) break;
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + s * kABytes);
           const uint32_t b_base = smem_u32(sB + s * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = sw128_desc(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = sw128_desc(b_base + kk * 2048, BK * 128, 1024);
-            mma_bf16(tmem, ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t ad = smem_desc(a_base + kk * 32, 16, 512, 4);
+            for (int h = 0; h < n_half; ++h) {
+              const uint64_t bd =
+                  smem_desc(b_base + h * (4 * kBBoxBytes) + kk * 2048, kBBoxBytes, 1024, 2);
+              mma_bf16(tmem + (uint32_t)(h * 256), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           mma_commit(&sh->empty[s]);
         }
@@ -328,80 +399,119 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ------------------------------------------------ p producers
-      const int pw = warp - 2;  // 0..3
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % NST;
-        const uint32_t use = (uint32_t)(i / NST);
-        if (i >= NST && !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status)) break;
-        uint8_t *tileA = sA + s * kABytes;
-        const int64_t k0 = (int64_t)(kb0 + i) * BK;
-        const int chunk = lane & 7;
-#pragma unroll 2
-        for (int it = 0; it < 8; ++it) {
-          const int r = pw * 32 + it * 4 + (lane >> 3);
-          uint4 packed = make_uint4(0u, 0u, 0u, 0u);
-          if (sh->row_ok[r]) {
-            const int64_t q = row0 + r;
-            const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
-            const char *rowp =
-                reinterpret_cast<const char *>(a.logits) + (size_t)q * (size_t)a.ld * esz;
-            const bool vec_ok = ((reinterpret_cast<uintptr_t>(rowp) & 15u) == 0);
-            float z[8];
-            load8(a, rowp, vec_ok, k0 + chunk * 8, z);
-            const float c = sh->row_c[r], l2 = sh->row_l2[r];
-            float p[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) p[j] = ex2_approx(fmaf(z[j], c, -l2));
-            packed.x = pack_bf16x2(p[0], p[1]);
-            packed.y = pack_bf16x2(p[2], p[3]);
-            packed.z = pack_bf16x2(p[4], p[5]);
-            packed.w = pack_bf16x2(p[6], p[7]);
-          }
-          const uint32_t off = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
-          *reinterpret_cast<uint4 *>(tileA + off) = packed;
+      const int t = threadIdx.x - 64;  // 0..255
+      // two (row, 16-byte chunk) units per thread, fixed across stages
+      const int r0 = t >> 2, r1 = r0 + 64, ch = t & 3;
+      const float c0 = sh->row_c[r0], l0 = sh->row_l2[r0];
+      const float c1 = sh->row_c[r1], l1 = sh->row_l2[r1];
+      const bool ok0 = sh->row_ok[r0] != 0, ok1 = sh->row_ok[r1] != 0;
+      const uint32_t off0 = a_off(r0, ch), off1 = a_off(r1, ch);
+      if (a.tma_a) {
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NST;
+          const uint32_t par = (uint32_t)(i / NST) & 1u;
+          // the whole warp leaves together if the wait gives up
+          if (!__all_sync(0xFFFFFFFFu,
+                          mbar_wait(&sh->full[s], par, sh, a.status, where_code(2, 0, s, i))))
+            break;
+          uint8_t *tileA = sA + s * kABytes;
+          const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
+          const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
+          uint4 *u0 = reinterpret_cast<uint4 *>(tileA + off0);
+          uint4 *u1 = reinterpret_cast<uint4 *>(tileA + off1);
+          const uint4 v0 = *u0, v1 = *u1;
+          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+          *u0 = ok0 ? p_from_bf16(w0, c0, l0, valid) : make_uint4(0u, 0u, 0u, 0u);
+          *u1 = ok1 ? p_from_bf16(w1, c1, l1, valid) : make_uint4(0u, 0u, 0u, 0u);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->a_ready[s]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->full_a[s]);
+      } else {
+        const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
+        const char *rp0 =
+            reinterpret_cast<const char *>(a.logits) + (size_t)(row0 + r0) * (size_t)a.ld * esz;
+        const char *rp1 =
+            reinterpret_cast<const char *>(a.logits) + (size_t)(row0 + r1) * (size_t)a.ld * esz;
+        Raw8 x0, x1;
+        if (nkb > 0) {
+          const int64_t k = (int64_t)kb0 * BK + ch * 8;
+          if (ok0) x0 = load_raw8(a, rp0, k);
+          if (ok1) x1 = load_raw8(a, rp1, k);
+        }
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NST;
+          const uint32_t use = (uint32_t)(i / NST);
+          if (i >= NST &&
+              !__all_sync(0xFFFFFFFFu, mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status,
+                                                 where_code(2, 2, s, i))))
+            break;
+          uint8_t *tileA = sA + s * kABytes;
+          const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
+          const int64_t rem = (int64_t)a.V - k;
+          const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
+          uint4 p0 = make_uint4(0u, 0u, 0u, 0u), p1 = p0;
+          if (a.dtype == DG_BF16) {
+            const uint32_t w0[4] = {x0.w[0], x0.w[1], x0.w[2], x0.w[3]};
+            const uint32_t w1[4] = {x1.w[0], x1.w[1], x1.w[2], x1.w[3]};
+            if (ok0) p0 = p_from_bf16(w0, c0, l0, valid);
+            if (ok1) p1 = p_from_bf16(w1, c1, l1, valid);
+          } else {
+            if (ok0) p0 = p_from_f32(x0.w, c0, l0, valid);
+            if (ok1) p1 = p_from_f32(x1.w, c1, l1, valid);
+          }
+          // prefetch the next stage's logits while this one is consumed
+          if (i + 1 < nkb) {
+            if (ok0) x0 = load_raw8(a, rp0, k + BK);
+            if (ok1) x1 = load_raw8(a, rp1, k + BK);
+          }
+          *reinterpret_cast<uint4 *>(tileA + off0) = p0;
+          *reinterpret_cast<uint4 *>(tileA + off1) = p1;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->a_ready[s]);
+        }
       }
     }
   }
 
   // ---------------------------------------------------- epilogue
   if (warp >= 2) {
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;         // which 256 accumulator columns
     const int r = quarter * 32 + lane;
     const int64_t q = row0 + r;
     bool have = false;
-    if (run) have = mbar_wait(&sh->tmem_full, 0, sh, a.status);
+    if (run) have = mbar_wait(&sh->tmem_full, 0, sh, a.status, where_code(3, 3, 0, 0));
     have = __all_sync(0xFFFFFFFFu, have);
     tc_fence_after();
     const bool ok = have && sh->row_ok[r] != 0;
-    for (int cb = 0; cb < BN; cb += 32) {
+    for (int cb = half * 256; cb < half * 256 + 256; cb += 32) {
+      const int col0 = n0 + cb;
+      if (col0 >= a.d) break;  // warp-uniform
       float v[32];
       if (have) {
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cb, v);
       }
-      if (q >= a.rows) continue;
-      const int col0 = n0 + cb;
-      if (col0 >= a.d) continue;
+      // per-lane conditions guard only the stores, never the warp-wide TMEM loads
       const int ncol = min(32, a.d - col0);
       if (!ok) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
       }
-      if (a.splits > 1) {
-        if (!run) continue;  // the reduction writes zeros for rows that do not feed
+      if (q < a.rows && a.splits > 1 && run) {
+        // (rows that do not feed get zeros from the reduction)
         float *dst = a.partial + ((size_t)split * a.rows + q) * a.d + col0;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           if (j < ncol) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      } else if (a.out_dtype == DG_F32) {
+      } else if (q < a.rows && a.splits == 1 && a.out_dtype == DG_F32) {
         float *dst = reinterpret_cast<float *>(a.out) + (size_t)q * a.d + col0;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
           if (j < ncol) *reinterpret_cast<float4 *>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      } else {
+      } else if (q < a.rows && a.splits == 1) {
         __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(a.out) + (size_t)q * a.d + col0;
 #pragma unroll
         for (int j = 0; j < 32; j += 8)
@@ -473,21 +583,28 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
+cudaError_t dg_selfcond_wait_record(uint32_t out[4]) {
+  return cudaMemcpyFromSymbol(out, g_wait_record, sizeof(uint32_t) * 4);
+}
+
 SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
   SelfcondPlan pl;
   pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
   pl.n_tiles = (d + BN - 1) / BN;
   pl.k_blocks = (V + BK - 1) / BK;
+  // work units in half tiles (the last column tile may be half wide)
+  const int64_t halves_per_m = (d + 255) / 256;
   const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
   // Choose the split count whose CTA count fills the SMs best (waves of
-  // kAssumedSMs), keeping at least 8 k-blocks per split.
+  // kAssumedSMs), keeping at least 16 k-blocks per split.
   int best = 1;
   double best_eff = 0.0;
-  for (int sp = 1; sp <= 32; ++sp) {
-    if (sp > 1 && pl.k_blocks / sp < 8) break;
+  for (int sp = 1; sp <= 64; ++sp) {
+    if (sp > 1 && pl.k_blocks / sp < 16) break;
     const int64_t ctas = tiles * sp;
     const int64_t waves = (ctas + kAssumedSMs - 1) / kAssumedSMs;
-    const double eff = (double)ctas / (double)(waves * kAssumedSMs);
+    const double work = (double)pl.m_tiles * (double)halves_per_m * 0.5 * sp;
+    const double eff = work / (double)(waves * kAssumedSMs);
     if (eff > best_eff + 0.05) {
       best_eff = eff;
       best = sp;
@@ -505,15 +622,32 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
                             void *ws, const SelfcondPlan &plan, cudaStream_t s) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
-  const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)BK};
-  const cuuint32_t estr[2] = {1, 1};
-  if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(E), dims, strides, box,
-          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return cudaErrorInvalidValue;
+  const int64_t rows = (int64_t)p.batch * p.canvas_len;
+  CUtensorMap map_e, map_z;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)BK};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(E), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const bool tma_a = p.logits_dtype == DG_BF16 &&
+                     (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
+                     (p.logits_ld * 2) % 16 == 0;
+  memset(&map_z, 0, sizeof(map_z));
+  if (tma_a) {
+    const cuuint64_t dims[2] = {(cuuint64_t)p.vocab, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)p.logits_ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(logits), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
 
   GemmArgs a;
   a.logits = logits;
@@ -522,11 +656,13 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.C = p.canvas_len;
   a.d = d;
   a.dtype = p.logits_dtype;
-  a.rows = (int64_t)p.batch * p.canvas_len;
+  a.rows = rows;
+  a.m_tiles = plan.m_tiles;
   a.n_tiles = plan.n_tiles;
   a.splits = plan.splits;
   a.k_blocks = plan.k_blocks;
   a.kb_per_split = plan.kb_per_split;
+  a.tma_a = tma_a ? 1 : 0;
   a.phase = st.phase;
   a.sc_valid = st.sc_valid;
   a.temperature = st.temperature;
@@ -548,7 +684,7 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
-  selfcond_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map, a);
+  selfcond_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map_e, map_z, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {

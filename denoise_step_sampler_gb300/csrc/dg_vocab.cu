@@ -69,16 +69,35 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   one(L.S1, L.T1);
 }
 
-// Element-wise evaluation of group g (n members, z[0..n) finite or -inf).
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, off));
+  return x;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Element-wise evaluation of group g (n members, z[0..n) finite or -inf)
+// against the screening bound sb (a score some element already attains).
+// Only members whose own bound E_j >= X/n can still reach sb draw their
+// exponential and take a logarithm.
 __device__ __forceinline__ void gumbel_group_exact(const float *z, int n, uint32_t g, uint32_t h,
-                                                   float c, const Keys &K, Lane &L) {
+                                                   float c, float sb, const Keys &K, Lane &L) {
   const float X = exp1_draw(h);
-  const uint32_t J = below(fmix32(K.kb ^ g), (uint32_t)n);
   const float base = X / (float)n;
+  const uint32_t J = below(fmix32(K.kb ^ g), (uint32_t)n);
   for (int j = 0; j < n; ++j) {
+    // E_j >= base, so score_j <= z_j c - log2(base); skip if that is below sb
+    if (base > ex2_approx(fmaf(z[j], c, -sb)) * 1.001f) continue;
     float E = base;
     if ((uint32_t)j != J) E += exp1_draw(fmix32(K.kc ^ (g * kGroup + (uint32_t)j)));
-    const float sc = fmaf(z[j], c, -log2f(E));
+    const float sc = fmaf(z[j], c, -__log2f(E));
     if (sc > L.b2) {
       L.b2 = sc;
       L.cand = (int32_t)(g * kGroup + j);
@@ -87,8 +106,8 @@ __device__ __forceinline__ void gumbel_group_exact(const float *z, int n, uint32
 }
 
 // Fast path for a full group of 8 finite logits.
-__device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c, const Keys &K,
-                                       Lane &L) {
+__device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c, float sb,
+                                       const Keys &K, Lane &L) {
   const float vmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
                            fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
   if (vmax > L.zmax) {
@@ -122,12 +141,12 @@ __device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c,
     L.T0 = fma2(a2, e2, L.T0);
     L.T1 = fma2(a3, e3, L.T1);
   }
-  // Screen: the group can hold a score >= best only if its minimum
-  // exponential X/8 <= 2^(vmax*c - b2); X >= W = 1 - U, W from ~h.
+  // Screen: the group can hold a score >= sb only if its minimum
+  // exponential X/8 <= 2^(vmax*c - sb); X >= W = 1 - U, W from ~h.
   const uint32_t h = fmix32(K.ka ^ g);
   const float w = (float)(~h) * 2.3283064365386963e-10f;
-  const float thr = 8.0f * ex2_approx(fmaf(vmax, c, -L.b2));
-  if (w <= thr * 1.001f) gumbel_group_exact(z, 8, g, h, c, K, L);
+  const float thr = 8.0f * ex2_approx(fmaf(vmax, c, -sb));
+  if (w <= thr * 1.001f) gumbel_group_exact(z, 8, g, h, c, sb, K, L);
 }
 
 // Careful path for any group (n <= 8 members, any values): flags NaN / +inf,
@@ -170,15 +189,7 @@ __device__ void group_careful(const float *z, int n, uint32_t g, float c, const 
   }
   L.S0 = add2(L.S0, pack2(s, 0.f));
   L.T0 = add2(L.T0, pack2(t, 0.f));
-  gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, K, L);
-}
-
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+  gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, L.b2, K, L);
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&z)[8]) {
@@ -304,59 +315,69 @@ __global__ void __launch_bounds__(kWarps * 32)
   lane_init(L);
   uint32_t flags = 0;
 
-  // ---- fast path over full groups
-  if (aligned) {
-    if (DT == DG_BF16) {
-      const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
-      int q = lane;
-      for (; q + 3 * 32 < n_full; q += 4 * 32) {
-        uint4 v[4];
+  // ---- fast path over full groups.  Lanes walk the chunk in warp-uniform
+  // rounds (every lane runs the same number of iterations, so the warp-wide
+  // refresh of the screening bound is reached by all 32 lanes); the last,
+  // partial round is predicated per lane.
+  float wb = -INFINITY;  // best score attained anywhere in the warp so far
+  if (aligned && DT == DG_BF16) {
+    const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
+    const int rounds = n_full / 128;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int q = rd * 128 + lane;
+      uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = ld_stream(vrow + q + u * 32);
+      for (int u = 0; u < 4; ++u) v[u] = ld_stream(vrow + q + u * 32);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float z[8];
-          unpack_bf16x8(v[u], z);
-          group8(z, g0 + (uint32_t)(q + u * 32), c, K, L);
-        }
-      }
-      for (; q < n_full; q += 32) {
+      for (int u = 0; u < 4; ++u) {
         float z[8];
-        unpack_bf16x8(ld_stream(vrow + q), z);
-        group8(z, g0 + (uint32_t)q, c, K, L);
+        unpack_bf16x8(v[u], z);
+        group8(z, g0 + (uint32_t)(q + u * 32), c, fmaxf(wb, L.b2), K, L);
       }
-    } else {
-      const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
-      int q = lane;
-      for (; q + 1 * 32 < n_full; q += 2 * 32) {
-        uint4 v[4];
+      wb = warp_max(fmaxf(wb, L.b2));
+    }
+    for (int q = rounds * 128 + lane; q < n_full; q += 32) {
+      float z[8];
+      unpack_bf16x8(ld_stream(vrow + q), z);
+      group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
+    }
+  } else if (aligned) {
+    const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
+    const int rounds = n_full / 64;
+    for (int rd = 0; rd < rounds; ++rd) {
+      const int q = rd * 64 + lane;
+      uint4 v[4];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          v[2 * u] = ld_stream(vrow + 2 * (q + u * 32));
-          v[2 * u + 1] = ld_stream(vrow + 2 * (q + u * 32) + 1);
-        }
+      for (int u = 0; u < 2; ++u) {
+        v[2 * u] = ld_stream(vrow + 2 * (q + u * 32));
+        v[2 * u + 1] = ld_stream(vrow + 2 * (q + u * 32) + 1);
+      }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          float z[8] = {__uint_as_float(v[2 * u].x),     __uint_as_float(v[2 * u].y),
-                        __uint_as_float(v[2 * u].z),     __uint_as_float(v[2 * u].w),
-                        __uint_as_float(v[2 * u + 1].x), __uint_as_float(v[2 * u + 1].y),
-                        __uint_as_float(v[2 * u + 1].z), __uint_as_float(v[2 * u + 1].w)};
-          group8(z, g0 + (uint32_t)(q + u * 32), c, K, L);
-        }
+      for (int u = 0; u < 2; ++u) {
+        float z[8] = {__uint_as_float(v[2 * u].x),     __uint_as_float(v[2 * u].y),
+                      __uint_as_float(v[2 * u].z),     __uint_as_float(v[2 * u].w),
+                      __uint_as_float(v[2 * u + 1].x), __uint_as_float(v[2 * u + 1].y),
+                      __uint_as_float(v[2 * u + 1].z), __uint_as_float(v[2 * u + 1].w)};
+        group8(z, g0 + (uint32_t)(q + u * 32), c, fmaxf(wb, L.b2), K, L);
       }
-      for (; q < n_full; q += 32) {
-        const uint4 a = ld_stream(vrow + 2 * q), b = ld_stream(vrow + 2 * q + 1);
-        float z[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
-                      __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
-                      __uint_as_float(b.z), __uint_as_float(b.w)};
-        group8(z, g0 + (uint32_t)q, c, K, L);
-      }
+      wb = warp_max(fmaxf(wb, L.b2));
+    }
+    for (int q = rounds * 64 + lane; q < n_full; q += 32) {
+      const uint4 a = ld_stream(vrow + 2 * q), b = ld_stream(vrow + 2 * q + 1);
+      float z[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                    __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
+                    __uint_as_float(b.z), __uint_as_float(b.w)};
+      group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
     }
   } else {
-    for (int q = lane; q < n_full; q += 32) {
-      float z[8];
-      load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
-      group8(z, g0 + (uint32_t)q, c, K, L);
+    for (int base = 0; base < n_full; base += 32) {  // warp-uniform trip count
+      const int q = base + lane;
+      if (q < n_full) {
+        float z[8];
+        load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
+        group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
+      }
+      if ((base & 127) == 96) wb = warp_max(fmaxf(wb, L.b2));
     }
   }
 

@@ -160,6 +160,14 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
 int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
               cudaStream_t stream);
 
+/* Diagnostics: copies to host memory the first bounded wait of the self-cond
+ * GEMM that gave up since the library was loaded, as {set, block, where,
+ * parity}; set = 0 if none did.  where = role << 28 | barrier << 24 |
+ * stage << 16 | k-iteration (roles 0 TMA, 1 MMA, 2 producer, 3 epilogue;
+ * barriers 0 full, 1 a_ready, 2 empty, 3 tmem_full).  Synchronous; not for
+ * use inside a captured graph. */
+int dg_debug_wait_record(uint32_t out[4]);
+
 /* Static description of a return code. */
 const char *dg_status_string(int code);
 
