@@ -22,7 +22,7 @@ __all__ = [
     "DG_DEV_BAD_TOKEN", "DG_DEV_WAIT_TIMEOUT", "DG_DEV_BAD_PHASE",
     "Params", "State", "DgError", "lib", "library_path",
     "dg_workspace_bytes", "dg_init_canvas", "dg_denoise_step", "dg_selfcond_embed",
-    "dg_commit", "dg_status_string",
+    "dg_commit", "dg_status_string", "dg_debug_wait_record",
 ]
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_WORKSPACE, DG_ERR_CUDA = 0, 1, 2, 3, 4
@@ -86,6 +86,8 @@ def lib():
         L.dg_selfcond_embed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
         L.dg_selfcond_embed.restype = ctypes.c_int
         L.dg_status_string.argtypes, L.dg_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+        L.dg_debug_wait_record.argtypes = [vp]
+        L.dg_debug_wait_record.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -200,6 +202,14 @@ def _ptr(t: torch.Tensor | None):
 
 def dg_status_string(code: int) -> str:
     return lib().dg_status_string(int(code)).decode()
+
+
+def dg_debug_wait_record() -> list:
+    """{set, block, where, parity} of the first self-cond GEMM wait that gave up
+    since load (diagnostics; synchronous)."""
+    rec = (ctypes.c_uint32 * 4)()
+    _check(lib().dg_debug_wait_record(ctypes.cast(rec, ctypes.c_void_p)), "dg_debug_wait_record")
+    return list(rec)
 
 
 def dg_workspace_bytes(params: Params, d: int = 0) -> int:

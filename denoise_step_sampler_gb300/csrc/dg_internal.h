@@ -29,6 +29,8 @@ struct SelfcondPlan {
   int32_t splits;    // K splits over the vocabulary
   int32_t k_blocks;  // ceil(V / BK)
   int32_t kb_per_split;  // k-blocks per split (every split non-empty)
+  int32_t cluster;   // CTAs per cluster sharing E tiles by multicast (1, 2 or 4)
+  int32_t m_groups;  // ceil(m_tiles / cluster)
   size_t ws_bytes;   // split-K partial sums (0 if splits == 1)
 };
 SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d);

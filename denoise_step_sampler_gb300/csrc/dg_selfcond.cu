@@ -43,10 +43,11 @@ constexpr int kAssumedSMs = 152;
 #endif
 constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
 
-struct Shared {
-  uint64_t full[NST];     // TMA bytes of the stage landed
-  uint64_t a_ready[NST];  // producers wrote p into the A tile
-  uint64_t empty[NST];    // the MMAs reading the stage completed
+template <int NS>
+struct SharedT {
+  uint64_t full[NS];     // TMA bytes of the stage landed
+  uint64_t a_ready[NS];  // producers wrote p into the A tile
+  uint64_t empty[NS];    // the MMAs reading the stage completed
   uint64_t tmem_full;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -56,6 +57,7 @@ struct Shared {
   float row_l2[BM];
   int32_t row_ok[BM];
 };
+using Shared = SharedT<NST>;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -101,13 +103,20 @@ __device__ __forceinline__ uint32_t where_code(uint32_t role, uint32_t bar, int 
 }
 
 // Bounded wait; false if it gave up or another role aborted.
-__device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Shared *sh,
-                                       uint32_t *status, uint32_t where) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try(b, parity)) {
-    if (*(volatile int32_t *)&sh->abort_flag) return false;
-    if (globaltimer() - t0 > kWaitNs) {
-      *(volatile int32_t *)&sh->abort_flag = 1;
+__device__ __noinline__ bool mbar_wait_flag(uint64_t *b, uint32_t parity, int32_t *abort_flag,
+                                            uint32_t *status, uint32_t where) {
+  // Poll the barrier; only every 256th failed poll looks at the abort flag and
+  // the clock, so a completed phase is noticed at once.
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(b, parity)) return true;
+    if ((it & 255u) != 0u) continue;
+    if (*(volatile int32_t *)abort_flag) return false;
+    const uint64_t now = globaltimer();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > kWaitNs) {
+      *(volatile int32_t *)abort_flag = 1;
       atomicOr(status, (uint32_t)DG_DEV_WAIT_TIMEOUT);
       if (atomicCAS(&g_wait_record[0], 0u, 1u) == 0u) {
         g_wait_record[1] = blockIdx.x;
@@ -117,13 +126,21 @@ __device__ __noinline__ bool mbar_wait(uint64_t *b, uint32_t parity, Shared *sh,
       return false;
     }
   }
-  return true;
+}
+template <class SH>
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, SH *sh, uint32_t *status,
+                                          uint32_t where) {
+  return mbar_wait_flag(b, parity, &sh->abort_flag, status, where);
 }
 // Bounded wait used while draining after an abort (ignores the abort flag).
 __device__ __noinline__ void mbar_drain(uint64_t *b, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
-  while (!mbar_try(b, parity)) {
-    if (globaltimer() - t0 > kWaitNs) return;
+  uint64_t t0 = 0;
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(b, parity)) return;
+    if ((it & 255u) != 0u) continue;
+    const uint64_t now = globaltimer();
+    if (t0 == 0) t0 = now;
+    else if (now - t0 > kWaitNs) return;
   }
 }
 
@@ -160,6 +177,43 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
 }
+// Multicast TMA load: the box lands at the same shared-memory offset in every
+// CTA of `mask`, completing bytes on each one's barrier at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                               int32_t x, int32_t y, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+// Arrive (once) on the barrier at `bar`'s offset in every CTA of `mask` when
+// the MMAs issued so far by this thread complete.
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Load a 32-bit word at `p`'s shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ int32_t ld_peer_i32(const void *p, uint32_t rank) {
+  uint32_t addr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -200,6 +254,7 @@ struct GemmArgs {
   int32_t V, C, d, dtype;
   int64_t rows;  // B*C
   int32_t m_tiles, n_tiles, splits, k_blocks, kb_per_split;
+  int32_t m_groups;  // ceil(m_tiles / cluster size)
   int32_t tma_a;  // 1: bf16 logits tiles arrive by TMA; 0: producers load them
   const uint8_t *phase;
   const uint8_t *sc_valid;
@@ -291,6 +346,10 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
   return (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
 }
 
+// CL CTAs form a cluster over CL consecutive row tiles of one column tile and
+// one vocabulary split: each loads 1/CL of every E tile and multicasts it to
+// all CL, so E leaves L2 once per cluster instead of once per CTA.
+template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
                          const __grid_constant__ CUtensorMap tmap_z, GemmArgs a) {
@@ -302,11 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared *sh = reinterpret_cast<Shared *>(smem + NST * (kABytes + kBBytes));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x;
-  const int n_t = tile % a.n_tiles;
-  const int rest = tile / a.n_tiles;
-  const int m_t = rest % a.m_tiles;
-  const int split = rest / a.m_tiles;
+  const int rank = (CL > 1) ? (int)cluster_rank() : 0;
+  const int cl = blockIdx.x / CL;
+  const int n_t = cl % a.n_tiles;
+  const int rest = cl / a.n_tiles;
+  const int m_t = (rest % a.m_groups) * CL + rank;
+  const int split = rest / a.m_groups;
+  const uint16_t cl_mask = (uint16_t)((1u << CL) - 1u);
   const int64_t row0 = (int64_t)m_t * BM;
   const int n0 = n_t * BN;
   const int kb0 = split * a.kb_per_split;
@@ -320,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sh->full[s], 1);
       mbar_init(&sh->a_ready[s], kProdWarps);
-      mbar_init(&sh->empty[s], 1);
+      mbar_init(&sh->empty[s], CL);  // one MMA-commit arrival from each CTA of the cluster
     }
     mbar_init(&sh->tmem_full, 1);
     mbar_init(&sh->mma_done, 1);
@@ -345,9 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  const bool run = sh->any_valid != 0 && nkb > 0;
+  // the cluster runs its pipeline if any of its CTAs has a row to feed
+  int32_t any = 0;
+#pragma unroll
+  for (int r = 0; r < CL; ++r) any |= (CL > 1) ? ld_peer_i32(&sh->any_valid, (uint32_t)r) : sh->any_valid;
+  const bool run = any != 0 && nkb > 0;
 
   if (run) {
     if (warp == 0) {
@@ -363,8 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_expect_tx(&sh->full[s], stage_tx);
           const int32_t kv = (kb0 + i) * BK;
           uint8_t *dstB = sB + s * kBBytes;
-          for (int j = 0; j < n_box; ++j)
-            tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
+          for (int j = 0; j < n_box; ++j) {
+            if (CL == 1)
+              tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
+            else if (j % CL == rank)
+              tma_load_2d_mc(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv,
+                             cl_mask);
+          }
           if (a.tma_a) tma_load_2d(sA + s * kABytes, &tmap_z, &sh->full[s], kv, (int32_t)row0);
           issued = i + 1;
         }
@@ -392,7 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16(tmem + (uint32_t)(h * 256), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          mma_commit(&sh->empty[s]);
+          if (CL == 1)
+            mma_commit(&sh->empty[s]);
+          else
+            mma_commit_mc(&sh->empty[s], cl_mask);  // every CTA may now reuse stage s
         }
         mma_commit(&sh->tmem_full);
         mma_commit(&sh->mma_done);
@@ -531,6 +605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN));
   }
+  // no CTA leaves while a peer may still signal its barriers or write its
+  // shared memory
+  if (CL > 1) cluster_sync_all();
 }
 
 // out[q, :] = sum over splits of the partial sums, zeros for rows that do
@@ -592,9 +669,14 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
   pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
   pl.n_tiles = (d + BN - 1) / BN;
   pl.k_blocks = (V + BK - 1) / BK;
+  // clusters of 2 row tiles share every E tile (multicast); a lone row tile
+  // runs alone
+  pl.cluster = pl.m_tiles >= 2 ? 2 : 1;
+  pl.m_groups = (pl.m_tiles + pl.cluster - 1) / pl.cluster;
+  const int64_t m_pad = (int64_t)pl.m_groups * pl.cluster;
   // work units in half tiles (the last column tile may be half wide)
   const int64_t halves_per_m = (d + 255) / 256;
-  const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
+  const int64_t tiles = m_pad * pl.n_tiles;
   // Choose the split count whose CTA count fills the SMs best (waves of
   // kAssumedSMs), keeping at least 16 k-blocks per split.
   int best = 1;
@@ -616,6 +698,38 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
   pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0;
   return pl;
 }
+
+namespace {
+template <int CL>
+cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z, const GemmArgs &a,
+                        int64_t grid, cudaStream_t s) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL>, map_e, map_z, a);
+}
+
+}  // namespace
 
 cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
@@ -658,6 +772,7 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.dtype = p.logits_dtype;
   a.rows = rows;
   a.m_tiles = plan.m_tiles;
+  a.m_groups = plan.m_groups;
   a.n_tiles = plan.n_tiles;
   a.splits = plan.splits;
   a.k_blocks = plan.k_blocks;
@@ -673,18 +788,13 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.partial = reinterpret_cast<float *>(ws);
   a.status = st.device_status;
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  const int64_t grid = (int64_t)plan.m_groups * plan.cluster * plan.n_tiles * plan.splits;
+  cudaError_t e;
+  if (plan.cluster == 2)
+    e = launch_gemm<2>(map_e, map_z, a, grid, s);
+  else
+    e = launch_gemm<1>(map_e, map_z, a, grid, s);
   if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {false};
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(selfcond_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
-  }
-  const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
-  selfcond_gemm_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map_e, map_z, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {

@@ -69,12 +69,6 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   one(L.S1, L.T1);
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, off));
-  return x;
-}
-
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -105,9 +99,12 @@ __device__ __forceinline__ void gumbel_group_exact(const float *z, int n, uint32
   }
 }
 
-// Fast path for a full group of 8 finite logits.
-__device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c, float sb,
-                                       const Keys &K, Lane &L) {
+// Fast path for a full group of 8 finite logits: max / argmax and the
+// softmax sums; returns whether the group passes the Gumbel screen against sb
+// (its minimum exponential X/8 <= 2^(vmax*c - sb); X >= W = 1 - U with W
+// from ~h), with the group's draw in h.
+__device__ __forceinline__ bool group8(const float (&z)[8], uint32_t g, float c, float sb,
+                                       const Keys &K, Lane &L, uint32_t &h) {
   const float vmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
                            fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
   if (vmax > L.zmax) {
@@ -141,12 +138,63 @@ __device__ __forceinline__ void group8(const float (&z)[8], uint32_t g, float c,
     L.T0 = fma2(a2, e2, L.T0);
     L.T1 = fma2(a3, e3, L.T1);
   }
-  // Screen: the group can hold a score >= sb only if its minimum
-  // exponential X/8 <= 2^(vmax*c - sb); X >= W = 1 - U, W from ~h.
-  const uint32_t h = fmix32(K.ka ^ g);
+  h = fmix32(K.ka ^ g);
   const float w = (float)(~h) * 2.3283064365386963e-10f;
   const float thr = 8.0f * ex2_approx(fmaf(vmax, c, -sb));
-  if (w <= thr * 1.001f) gumbel_group_exact(z, 8, g, h, c, sb, K, L);
+  return w <= thr * 1.001f;
+}
+
+// Warp-cooperative exact evaluation of the groups that passed the screen
+// (one flag per lane, all 32 lanes call this).  Up to four passing groups
+// are evaluated at a time, eight lanes per group and one member per lane, so
+// the rare exact draws run convergently instead of one lane at a time.  Each
+// evaluating lane keeps the best (score, index) it saw; the warp merge at the
+// end takes the overall maximum, lowest index on ties.  The warp-wide bound
+// wb is refreshed afterwards.
+__device__ __forceinline__ void coop_eval(bool pass, const float (&z)[8], uint32_t g, uint32_t h,
+                                          float c, float &wb, const Keys &K, Lane &L, int lane) {
+  uint32_t mask = __ballot_sync(0xFFFFFFFFu, pass);
+  if (mask == 0u) return;
+  const int slot = lane >> 3, j = lane & 7;
+  const float sb = wb;
+  while (mask != 0u) {
+    uint32_t mm = mask;
+    int owner = -1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int bit = mm ? (__ffs(mm) - 1) : -1;
+      if (k == slot) owner = bit;
+      if (mm) mm &= mm - 1u;
+    }
+    mask = mm;
+    const int src = owner >= 0 ? owner : lane;
+    float zj = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const float v = __shfl_sync(0xFFFFFFFFu, z[jj], src);
+      if (jj == j) zj = v;
+    }
+    const uint32_t gg = __shfl_sync(0xFFFFFFFFu, g, src);
+    const uint32_t hh = __shfl_sync(0xFFFFFFFFu, h, src);
+    if (owner >= 0) {
+      const float base = exp1_draw(hh) * 0.125f;
+      // E_j >= X/8, so score_j <= z_j c - log2(X/8): skip if below sb
+      if (!(base > ex2_approx(fmaf(zj, c, -sb)) * 1.001f)) {
+        const uint32_t J = below(fmix32(K.kb ^ gg), 8u);
+        float E = base;
+        if ((uint32_t)j != J) E += exp1_draw(fmix32(K.kc ^ (gg * kGroup + (uint32_t)j)));
+        const float sc = fmaf(zj, c, -__log2f(E));
+        const int32_t idx = (int32_t)(gg * kGroup + (uint32_t)j);
+        if (sc > L.b2 || (sc == L.b2 && (uint32_t)idx < (uint32_t)L.cand)) {
+          L.b2 = sc;
+          L.cand = idx;
+        }
+      }
+    }
+  }
+  wb = fmaxf(wb, L.b2);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
 }
 
 // Careful path for any group (n <= 8 members, any values): flags NaN / +inf,
@@ -316,9 +364,9 @@ __global__ void __launch_bounds__(kWarps * 32)
   uint32_t flags = 0;
 
   // ---- fast path over full groups.  Lanes walk the chunk in warp-uniform
-  // rounds (every lane runs the same number of iterations, so the warp-wide
-  // refresh of the screening bound is reached by all 32 lanes); the last,
-  // partial round is predicated per lane.
+  // rounds (every lane runs the same number of iterations, partial rounds are
+  // predicated per lane), so the warp-cooperative steps are reached by all 32
+  // lanes.
   float wb = -INFINITY;  // best score attained anywhere in the warp so far
   if (aligned && DT == DG_BF16) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
@@ -332,14 +380,22 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int u = 0; u < 4; ++u) {
         float z[8];
         unpack_bf16x8(v[u], z);
-        group8(z, g0 + (uint32_t)(q + u * 32), c, fmaxf(wb, L.b2), K, L);
+        const uint32_t g = g0 + (uint32_t)(q + u * 32);
+        uint32_t h;
+        const bool pass = group8(z, g, c, wb, K, L, h);
+        coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
-      wb = warp_max(fmaxf(wb, L.b2));
     }
-    for (int q = rounds * 128 + lane; q < n_full; q += 32) {
+    for (int base = rounds * 128; base < n_full; base += 32) {
+      const int q = base + lane;
       float z[8];
-      unpack_bf16x8(ld_stream(vrow + q), z);
-      group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
+      uint32_t h = 0;
+      bool pass = false;
+      if (q < n_full) {
+        unpack_bf16x8(ld_stream(vrow + q), z);
+        pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
+      }
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
     }
   } else if (aligned) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
@@ -358,26 +414,38 @@ __global__ void __launch_bounds__(kWarps * 32)
                       __uint_as_float(v[2 * u].z),     __uint_as_float(v[2 * u].w),
                       __uint_as_float(v[2 * u + 1].x), __uint_as_float(v[2 * u + 1].y),
                       __uint_as_float(v[2 * u + 1].z), __uint_as_float(v[2 * u + 1].w)};
-        group8(z, g0 + (uint32_t)(q + u * 32), c, fmaxf(wb, L.b2), K, L);
+        const uint32_t g = g0 + (uint32_t)(q + u * 32);
+        uint32_t h;
+        const bool pass = group8(z, g, c, wb, K, L, h);
+        coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
-      wb = warp_max(fmaxf(wb, L.b2));
     }
-    for (int q = rounds * 64 + lane; q < n_full; q += 32) {
-      const uint4 a = ld_stream(vrow + 2 * q), b = ld_stream(vrow + 2 * q + 1);
-      float z[8] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
-                    __uint_as_float(a.w), __uint_as_float(b.x), __uint_as_float(b.y),
-                    __uint_as_float(b.z), __uint_as_float(b.w)};
-      group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
+    for (int base = rounds * 64; base < n_full; base += 32) {
+      const int q = base + lane;
+      float z[8];
+      uint32_t h = 0;
+      bool pass = false;
+      if (q < n_full) {
+        const uint4 a = ld_stream(vrow + 2 * q), b = ld_stream(vrow + 2 * q + 1);
+        z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
+        z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
+        z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
+        z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
+        pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
+      }
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
     }
   } else {
     for (int base = 0; base < n_full; base += 32) {  // warp-uniform trip count
       const int q = base + lane;
+      float z[8];
+      uint32_t h = 0;
+      bool pass = false;
       if (q < n_full) {
-        float z[8];
         load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
-        group8(z, g0 + (uint32_t)q, c, fmaxf(wb, L.b2), K, L);
+        pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      if ((base & 127) == 96) wb = warp_max(fmaxf(wb, L.b2));
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
     }
   }
 

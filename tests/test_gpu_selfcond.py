@@ -40,6 +40,8 @@ CASES = [
     (3, 64, 4096, dg.DG_BF16, None, 128, 128, torch.bfloat16),
     (1, 256, 20000, dg.DG_BF16, None, 512, 512, torch.float32),
     (4, 256, 3000, dg.DG_BF16, None, 768, 768, torch.float32),
+    (3, 128, 2048, dg.DG_BF16, None, 128, 128, torch.float32),   # odd row-tile count
+    (5, 256, 1024, dg.DG_F32, None, 1024, 1024, torch.float32),  # fp32, many row tiles
 ]
 
 
