@@ -22,10 +22,12 @@ __all__ = [
     "DG_DEV_BAD_TOKEN", "DG_DEV_WAIT_TIMEOUT", "DG_DEV_BAD_PHASE",
     "Params", "State", "DgError", "lib", "library_path",
     "dg_workspace_bytes", "dg_init_canvas", "dg_denoise_step", "dg_selfcond_embed",
-    "dg_commit", "dg_status_string", "dg_debug_wait_record",
+    "dg_commit", "dg_status_string", "dg_debug_wait_record", "dg_denoise_step_noalloc",
+    "DG_ERR_SCRATCH_LIMIT",
 ]
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_WORKSPACE, DG_ERR_CUDA = 0, 1, 2, 3, 4
+DG_ERR_SCRATCH_LIMIT = 5
 DG_PHASE_PREFILL, DG_PHASE_DENOISE, DG_PHASE_COMMIT, DG_PHASE_IDLE = 0, 1, 2, 3
 DG_F32, DG_BF16 = 0, 1
 DG_DEV_NONFINITE_LOGITS, DG_DEV_BAD_TEMPERATURE, DG_DEV_BAD_TOKEN = 1, 2, 4
@@ -86,6 +88,8 @@ def lib():
         L.dg_selfcond_embed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
         L.dg_selfcond_embed.restype = ctypes.c_int
         L.dg_status_string.argtypes, L.dg_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+        L.dg_denoise_step_noalloc.argtypes = [P, vp, S, vp]
+        L.dg_denoise_step_noalloc.restype = ctypes.c_int
         L.dg_debug_wait_record.argtypes = [vp]
         L.dg_debug_wait_record.restype = ctypes.c_int
         _LIB = L
@@ -245,6 +249,16 @@ def dg_denoise_step(params: Params, logits: torch.Tensor, state: State,
     _check(lib().dg_denoise_step(ctypes.byref(params.c()), _ptr(logits), ctypes.byref(state.c()),
                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _stream_ptr(stream)), "dg_denoise_step")
+
+
+def dg_denoise_step_noalloc(params: Params, logits: torch.Tensor, state: State, stream=None):
+    """dg_denoise_step for callers that cannot allocate device memory: no
+    workspace argument; the library's own fixed scratch is used instead (see
+    include/dg.h for its limit and sharing rules)."""
+    _logits_ok(params, logits)
+    _check(lib().dg_denoise_step_noalloc(ctypes.byref(params.c()), _ptr(logits),
+                                         ctypes.byref(state.c()), _stream_ptr(stream)),
+           "dg_denoise_step_noalloc")
 
 
 def dg_selfcond_embed(params: Params, logits: torch.Tensor, state: State, E: torch.Tensor,

@@ -168,6 +168,8 @@ const char *dg_status_string(int code) {
       return "workspace missing or too small";
     case DG_ERR_CUDA:
       return "CUDA error";
+    case DG_ERR_SCRATCH_LIMIT:
+      return "problem larger than the fixed scratch of dg_denoise_step_noalloc";
     default:
       return "unknown status";
   }

@@ -45,7 +45,8 @@ typedef enum {
   DG_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad alignment, bad enum   */
   DG_ERR_UNSUPPORTED = 2, /* device is not sm_103 / unsupported dtype combo    */
   DG_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required   */
-  DG_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed            */
+  DG_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed            */
+  DG_ERR_SCRATCH_LIMIT = 5 /* too large for dg_denoise_step_noalloc's fixed scratch */
 } dg_status;
 
 /* Sticky bits OR-ed into state->device_status[0] by the kernels. */
@@ -159,6 +160,24 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
  * counters reset, phase = DENOISE, rng_step += 1. */
 int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
               cudaStream_t stream);
+
+/* dg_denoise_step without a workspace, for callers that cannot allocate
+ * device memory (an engine whose device memory is all pre-planned by its own
+ * pool, or a host application whose allocations belong to another
+ * framework's allocator).  The sources describe no such variant; it exists
+ * for deployment only.  Same arguments, semantics and results as
+ * dg_denoise_step; the scratch it needs (one 32-byte record per position and
+ * vocabulary chunk) lives in a 2 MiB array inside the library that every GPU
+ * loading the library keeps until the process exits.  Limit: batch *
+ * canvas_len * chunks <= 65536 records (for example 32768 positions at
+ * V = 262144, or 2048 positions of 8 chunks each); larger problems return
+ * DG_ERR_SCRATCH_LIMIT before anything is enqueued.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Calls
+ * share the array, so two calls whose kernels may overlap on the GPU race:
+ * order them on one stream.  Allocates and frees nothing. */
+int dg_denoise_step_noalloc(const dg_params *p, const void *logits, const dg_state *st,
+                            cudaStream_t stream);
 
 /* Diagnostics: copies to host memory the first bounded wait of the self-cond
  * GEMM that gave up since the library was loaded, as {set, block, where,
