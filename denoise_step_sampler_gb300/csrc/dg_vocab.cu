@@ -27,11 +27,16 @@ struct Keys {
   uint32_t ka, kb, kc;  // low words of the GMIN / GARG / GREST stream keys
 };
 
+// The softmax sums are kept in three levels so that no fp32 sum adds more
+// than a few dozen terms: S/T collect one round of groups, BS/BT collect up
+// to 16 rounds, ts/tt the rest of the chunk.
 struct Lane {
   float zmax;   // running max of stored logits
   int32_t am;   // its lowest index
   float m2;     // fl(zmax * c)
-  uint64_t S0, S1, T0, T1;  // packed partial sums of 2^a and a 2^a
+  uint64_t S0, S1, T0, T1;      // packed round sums of 2^a and a 2^a
+  uint64_t BS, BT;              // packed block sums
+  float ts, tt;                 // chunk totals
   float b2;     // best perturbed score, base 2
   int32_t cand;
 };
@@ -41,22 +46,42 @@ __device__ __forceinline__ void lane_init(Lane &L) {
   L.am = -1;
   L.m2 = -INFINITY;
   L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+  L.BS = L.BT = 0ull;
+  L.ts = L.tt = 0.f;
   L.b2 = -INFINITY;
   L.cand = -1;
 }
 
-__device__ __forceinline__ void sums(const Lane &L, float &s, float &t) {
-  s = (lo2(L.S0) + hi2(L.S0)) + (lo2(L.S1) + hi2(L.S1));
-  t = (lo2(L.T0) + hi2(L.T0)) + (lo2(L.T1) + hi2(L.T1));
+// Round sums into the block sums.
+__device__ __forceinline__ void fold_round(Lane &L) {
+  L.BS = add2(L.BS, add2(L.S0, L.S1));
+  L.BT = add2(L.BT, add2(L.T0, L.T1));
+  L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+}
+// Block sums into the chunk totals.
+__device__ __forceinline__ void fold_block(Lane &L) {
+  fold_round(L);
+  L.ts += lo2(L.BS) + hi2(L.BS);
+  L.tt += lo2(L.BT) + hi2(L.BT);
+  L.BS = L.BT = 0ull;
 }
 
-// The running maximum moved from L.m2 to m2n: rescale the sums.
+__device__ __forceinline__ void sums(Lane &L, float &s, float &t) {
+  fold_block(L);
+  s = L.ts;
+  t = L.tt;
+}
+
+// The running maximum moved from L.m2 to m2n: rescale the sums of every
+// level (s' = s 2^d, t' = (t + d s) 2^d with d = m2 - m2n <= 0).
 __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   if (L.zmax == -INFINITY) {
     L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+    L.BS = L.BT = 0ull;
+    L.ts = L.tt = 0.f;
     return;
   }
-  const float d = L.m2 - m2n;  // <= 0
+  const float d = L.m2 - m2n;
   const float f = ex2_approx(d);
   auto one = [&](uint64_t &S, uint64_t &T) {
     float s0 = lo2(S), s1 = hi2(S), t0 = lo2(T), t1 = hi2(T);
@@ -67,6 +92,9 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   };
   one(L.S0, L.T0);
   one(L.S1, L.T1);
+  one(L.BS, L.BT);
+  L.tt = fmaf(d, L.ts, L.tt) * f;
+  L.ts *= f;
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -237,6 +265,7 @@ __device__ void group_careful(const float *z, int n, uint32_t g, float c, const 
   }
   L.S0 = add2(L.S0, pack2(s, 0.f));
   L.T0 = add2(L.T0, pack2(t, 0.f));
+  if ((g & 15u) == 15u) fold_block(L); else fold_round(L);
   gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, L.b2, K, L);
 }
 
@@ -309,7 +338,8 @@ __device__ __forceinline__ void warp_merge(float c, float &zmax, int32_t &am, fl
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kWarps * 32)
+// 4 CTAs of 8 warps per SM: the register budget is capped at 64 per thread
+__global__ void __launch_bounds__(kWarps * 32, 4)
     vocab_pass_kernel(const void *__restrict__ logits, int64_t ld, int32_t V, int32_t C,
                       int64_t n_pos, int32_t chunk, int32_t n_chunks, uint64_t seed,
                       const uint8_t *__restrict__ phase, const uint64_t *__restrict__ request_id,
@@ -385,6 +415,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         const bool pass = group8(z, g, c, wb, K, L, h);
         coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
+      if ((rd & 15) == 15) fold_block(L); else fold_round(L);
     }
     for (int base = rounds * 128; base < n_full; base += 32) {
       const int q = base + lane;
@@ -419,6 +450,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         const bool pass = group8(z, g, c, wb, K, L, h);
         coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
+      if ((rd & 15) == 15) fold_block(L); else fold_round(L);
     }
     for (int base = rounds * 64; base < n_full; base += 32) {
       const int q = base + lane;
@@ -446,6 +478,7 @@ __global__ void __launch_bounds__(kWarps * 32)
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
       coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
+      if ((base & 511) == 480) fold_block(L); else if ((base & 127) == 96) fold_round(L);
     }
   }
 
