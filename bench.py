@@ -46,6 +46,21 @@ METRIC = "denoise-step positions/s (sampler+self-cond)"
 SEED = 0xD1FF0002
 
 
+def traffic_for(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary of a kernel, only if
+    the kernel's source is unchanged since the capture (else None)."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            table = json.load(f)
+        ent = table[kernel_file]
+        src = os.path.join(ROOT, "denoise_step_sampler_gb300", "csrc", kernel_file)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["dram_bytes_per_launch"] if ent.get("source_sha256_16") == h else None
+    except Exception:
+        return None
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -241,32 +256,34 @@ def run_ours(args, rank, world, dev):
     ms_sc = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     status = int(st.device_status.item())
 
-    # end-to-end: host logits in pinned memory copied in, results copied out
-    host_logits = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
-    host_logits.copy_(logits)
-    dev_logits = torch.empty_like(logits)
-    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    host_canvas = torch.empty(st.canvas.shape, dtype=st.canvas.dtype, pin_memory=True)
-    for _ in range(max(1, args.warmup)):
-        dev_logits.copy_(host_logits, non_blocking=True)
-        step(dev_logits)
-        host_out.copy_(out, non_blocking=True)
-        host_canvas.copy_(st.canvas, non_blocking=True)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    Ke = max(1, K // 4)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(Ke):
-        dev_logits.copy_(host_logits, non_blocking=True)
-        step(dev_logits)
-        host_out.copy_(out, non_blocking=True)
-        host_canvas.copy_(st.canvas, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms_e2e = e0.elapsed_time(e1)
+    ms_e2e, Ke = float('nan'), 0
+    if not args.no_e2e:
+        # end-to-end: host logits in pinned memory copied in, results copied out
+        host_logits = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+        host_logits.copy_(logits)
+        dev_logits = torch.empty_like(logits)
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        host_canvas = torch.empty(st.canvas.shape, dtype=st.canvas.dtype, pin_memory=True)
+        for _ in range(max(1, args.warmup)):
+            dev_logits.copy_(host_logits, non_blocking=True)
+            step(dev_logits)
+            host_out.copy_(out, non_blocking=True)
+            host_canvas.copy_(st.canvas, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+        Ke = max(1, K // 4)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            dev_logits.copy_(host_logits, non_blocking=True)
+            step(dev_logits)
+            host_out.copy_(out, non_blocking=True)
+            host_canvas.copy_(st.canvas, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms_e2e = e0.elapsed_time(e1)
 
     if world > 1:
         tm = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
@@ -277,7 +294,7 @@ def run_ours(args, rank, world, dev):
         return None
     n_pos = B * C
     value = world * n_pos * K / (ms / 1e3)
-    e2e_value = world * n_pos * Ke / (ms_e2e / 1e3)
+    e2e_value = world * n_pos * Ke / (ms_e2e / 1e3) if Ke else None
     hbm, bf16, src = peaks()
     flops = 2.0 * n_pos * V * d
     sc_tflops = flops / (ms_sc / 1e3) / 1e12
@@ -299,12 +316,14 @@ def run_ours(args, rank, world, dev):
                    "parallelism": f"replicas x{world} (independent requests per GPU)"},
         "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
-                     "frac": sc_tflops / bf16, "traffic": None,
+                     "frac": sc_tflops / bf16,
+                     "traffic": traffic_for("dg_selfcond.cu") if args.workload == DEFAULT and not args.batch else None,
                      "peak_source": f"{src} bf16 burst", "flops_per_launch": flops,
                      "ms_per_launch": ms_sc},
         "roofline_sampler": {"bound": "hbm", "kernel": "dg_denoise_step (vocab pass + canvas step)",
                              "achieved": sampler_gbs, "peak": hbm, "unit": "GB/s",
-                             "frac": sampler_gbs / hbm, "traffic": None,
+                             "frac": sampler_gbs / hbm,
+                             "traffic": traffic_for("dg_vocab.cu") if args.workload == DEFAULT and not args.batch else None,
                              "peak_source": f"{src} copy", "bytes_per_launch": logit_bytes,
                              "ms_per_launch": ms_sampler},
         "clocks": clk,
@@ -342,6 +361,72 @@ def _selfcond_splits(rows, V, d):
             best, best_eff = sp, eff
     kbps = -(-k // best)
     return -(-k // kbps)
+
+
+def run_graph_loop(args, dev):
+    """One canvas, V = 262144, d = 2816: a block of 24 denoise steps and its
+    commit (25 calls of dg_denoise_step + dg_selfcond_embed), per-step logits
+    pre-generated in HBM.  Reports the per-step time eager and replayed from a
+    captured CUDA graph."""
+    import torch
+    import denoise_step_sampler_gb300 as dg
+    from denoise_step_sampler_gb300 import build as dgbuild
+    from denoise_step_sampler_gb300 import synthetic as syn
+
+    dgbuild.build()
+    C, V, d, steps = 256, 262144, 2816, 24
+    seed = 0xD1FF0005
+    p = dg.Params(batch=1, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=seed,
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=steps)
+    T = float(syn.temperatures(1, seed=seed, device="cpu")[0])
+    bufs = [syn.loop_logits(C, V, seed=seed, request=0, step=s, device=dev).reshape(-1)
+            for s in range(steps + 1)]
+    E = syn.embedding(V, d, seed=seed + 1, device=dev)
+    ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device=dev)
+    out = torch.empty((C, d), dtype=torch.float32, device=dev)
+    st = dg.State(1, C, dev)
+    st.temperature.fill_(T)
+    mask = torch.ones(1, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def block(s_):
+        dg.dg_init_canvas(p, st, mask, stream=s_)
+        for k in range(steps + 1):
+            dg.dg_denoise_step(p, bufs[k], st, ws, stream=s_)
+            dg.dg_selfcond_embed(p, bufs[k], st, E, out, ws, stream=s_)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            block(stream)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(3, args.steps // 25)
+    e0.record(stream)
+    for _ in range(reps):
+        block(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_ms = e0.elapsed_time(e1) / reps
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        block(stream)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0.record(torch.cuda.current_stream(dev))
+    for _ in range(reps):
+        g.replay()
+    e1.record(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    graph_ms = e0.elapsed_time(e1) / reps
+    calls = steps + 1
+    return {"metric": "denoise-step latency, 1 canvas loop (24 steps + commit)",
+            "value": graph_ms / calls * 1e3, "unit": "us/step (graph replay)",
+            "higher_is_better": False, "eager_us_per_step": eager_ms / calls * 1e3,
+            "graph_ms_per_block": graph_ms, "eager_ms_per_block": eager_ms, "blocks": reps,
+            "config": {"workload": "1x256-V262144-bf16-d2816 loop", "steps": steps,
+                       "cap": steps, "temperature": T},
+            "device_status": int(st.device_status.item())}
 
 
 # ---------------------------------------------------------- reference arm
@@ -410,6 +495,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
     ap.add_argument("--batch", type=int, default=0, help="override the canvas count (sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (sweeps)")
+    ap.add_argument("--mode", default="step", choices=["step", "graph-loop"],
+                    help="step: the throughput line (default); graph-loop: one-canvas loop latency")
     ap.add_argument("--cpu-oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -438,7 +526,10 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    line = run_ours(args, rank, world, dev)
+    if args.mode == "graph-loop":
+        line = run_graph_loop(args, dev) if rank == 0 else None
+    else:
+        line = run_ours(args, rank, world, dev)
     if line is not None:
         print(json.dumps(line))
     if world > 1:

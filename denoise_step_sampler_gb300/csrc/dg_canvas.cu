@@ -41,6 +41,7 @@ struct CanvasArgs {
   dg_state st;
   const Partial *part;
   int32_t n_chunks;
+  int32_t merge_threads;  // threads per position in the chunk merge (1, 2 or 4)
   int mode;
   const uint8_t *row_mask;
 };
@@ -51,6 +52,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   __shared__ uint8_t sacc[kMaxC];
   __shared__ double swarp[32];
   __shared__ double soff[32];
+  __shared__ float sH[kMaxC];
+  __shared__ int32_t sAm[kMaxC], sCand[kMaxC];
 
   const int r = blockIdx.x;
   const int tid = threadIdx.x;
@@ -107,58 +110,105 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   }
 
   // ------------------------------------------------------------ DENOISE
+  // Merge the chunk records of each position: mt threads per position (the
+  // blockDim.x / CP2 adjacent lanes), each over a strided subset of chunks,
+  // with the sums rescaled to a running maximum in fp32, then a shuffle merge.
   const float T = st.temperature[r];
   const float c = kLog2e / T;
-  bool valid = false;
-  float H = NAN;
-  int32_t am = 0, cand = 0;
-  if (tid < C) {
-    const Partial *P = a.part + (size_t)(base + tid) * a.n_chunks;
+  const int mt = a.merge_threads;
+  {
+    const int i = tid / mt, sub = tid % mt;
     uint32_t fl = 0;
-    float zmax = -INFINITY, b2 = -INFINITY;
+    float zmax = -INFINITY, b2 = -INFINITY, S = 0.f, Tt = 0.f;
     int32_t pam = -1, pcand = -1;
-    for (int ch = 0; ch < a.n_chunks; ++ch) {
-      const Partial q = P[ch];
-      fl |= q.flags;
-      if (q.zmax > zmax || (q.zmax == zmax && q.am >= 0 && (pam < 0 || q.am < pam))) {
-        zmax = q.zmax;
-        pam = q.am;
-      }
-      if (q.b2 > b2 || (q.b2 == b2 && q.cand >= 0 && (pcand < 0 || q.cand < pcand))) {
-        b2 = q.b2;
-        pcand = q.cand;
-      }
-    }
-    float m_out = NAN, s_out = NAN;
-    if (!(fl & (kPartNaN | kPartPInf | kPartBadT)) && zmax != -INFINITY && pam >= 0 &&
-        pcand >= 0) {
-      const double M2 = (double)(zmax * c);
-      double S = 0.0, Tt = 0.0;
-      for (int ch = 0; ch < a.n_chunks; ++ch) {
+    if (i < C) {
+      const Partial *P = a.part + (size_t)(base + i) * a.n_chunks;
+      for (int ch = sub; ch < a.n_chunks; ch += mt) {
         const Partial q = P[ch];
+        fl |= q.flags;
+        if (q.zmax > zmax || (q.zmax == zmax && q.am >= 0 && (pam < 0 || q.am < pam))) {
+          if (q.zmax > zmax && S > 0.f) {  // the running maximum grows
+            const float d = zmax * c - q.zmax * c;
+            const float f = exp2f(d);
+            Tt = fmaf(d, S, Tt) * f;
+            S *= f;
+          }
+          zmax = q.zmax;
+          pam = q.am;
+        }
         if (q.s > 0.f) {
-          const double d = (double)(q.zmax * c) - M2;
-          const double f = exp2(d);
-          S += (double)q.s * f;
-          Tt += ((double)q.t + d * (double)q.s) * f;
+          const float d = q.zmax * c - zmax * c;
+          const float f = exp2f(d);
+          S = fmaf(q.s, f, S);
+          Tt = fmaf(fmaf(d, q.s, q.t), f, Tt);
+        }
+        if (q.b2 > b2 || (q.b2 == b2 && q.cand >= 0 && (pcand < 0 || q.cand < pcand))) {
+          b2 = q.b2;
+          pcand = q.cand;
         }
       }
-      if (S > 0.0 && isfinite(S) && isfinite(Tt)) {
-        valid = true;
-        H = (float)(0.6931471805599453 * (log2(S) - Tt / S));
-        m_out = zmax / T;
-        s_out = (float)S;
-        am = pam;
-        cand = pcand;
+    }
+    for (int off = 1; off < mt; off <<= 1) {
+      const float oz = __shfl_xor_sync(0xFFFFFFFFu, zmax, off);
+      const int32_t oam = __shfl_xor_sync(0xFFFFFFFFu, pam, off);
+      const float os = __shfl_xor_sync(0xFFFFFFFFu, S, off);
+      const float ot = __shfl_xor_sync(0xFFFFFFFFu, Tt, off);
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, b2, off);
+      const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, pcand, off);
+      fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, off);
+      const float nz = fmaxf(zmax, oz);
+      if (nz != -INFINITY) {
+        float ns = 0.f, nt2 = 0.f;
+        if (S > 0.f) {
+          const float d = zmax * c - nz * c;
+          const float f = exp2f(d);
+          ns = S * f;
+          nt2 = fmaf(d, S, Tt) * f;
+        }
+        if (os > 0.f) {
+          const float d = oz * c - nz * c;
+          const float f = exp2f(d);
+          ns = fmaf(os, f, ns);
+          nt2 = fmaf(fmaf(d, os, ot), f, nt2);
+        }
+        S = ns;
+        Tt = nt2;
+      }
+      if (oz > zmax || (oz == zmax && oam >= 0 && (pam < 0 || oam < pam))) {
+        zmax = oz;
+        pam = oam;
+      }
+      if (ob > b2 || (ob == b2 && oc >= 0 && (pcand < 0 || oc < pcand))) {
+        b2 = ob;
+        pcand = oc;
       }
     }
-    if (!valid && !(fl & kPartBadT)) atomicOr(st.device_status, (uint32_t)DG_DEV_NONFINITE_LOGITS);
-    st.m[base + tid] = m_out;
-    st.s[base + tid] = s_out;
-    st.entropy[base + tid] = H;
-    st.argmax[base + tid] = am;
-    st.cand[base + tid] = cand;
+    if (i < C && sub == 0) {
+      bool ok = !(fl & (kPartNaN | kPartPInf | kPartBadT)) && zmax != -INFINITY && pam >= 0 &&
+                pcand >= 0 && S > 0.f && isfinite(S) && isfinite(Tt);
+      float Hf = NAN, m_out = NAN, s_out = NAN;
+      if (ok) {
+        Hf = (float)(0.6931471805599453 * (log2((double)S) - (double)Tt / (double)S));
+        m_out = zmax / T;
+        s_out = S;
+      } else if (!(fl & kPartBadT)) {
+        atomicOr(st.device_status, (uint32_t)DG_DEV_NONFINITE_LOGITS);
+      }
+      sH[i] = ok ? Hf : NAN;
+      sAm[i] = ok ? pam : 0;
+      sCand[i] = ok ? pcand : 0;
+      st.m[base + i] = m_out;
+      st.s[base + i] = s_out;
+      st.entropy[base + i] = Hf;
+      st.argmax[base + i] = ok ? pam : 0;
+      st.cand[base + i] = ok ? pcand : 0;
+    }
   }
+  __syncthreads();
+  const bool valid = (tid < C) && !isnan(sH[tid]);
+  const float H = (tid < C) ? sH[tid] : NAN;
+  const int32_t am = (tid < C) ? sAm[tid] : 0;
+  const int32_t cand = (tid < C) ? sCand[tid] : 0;
 
   // sort (H, i) ascending; invalid positions and padding sort last as +inf
   skey[tid] = valid ? H : INFINITY;
@@ -251,6 +301,13 @@ cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Par
                                cudaStream_t s) {
   int threads = 32;
   while (threads < p.canvas_len) threads <<= 1;
+  // spread the chunk merge over up to 4 threads per position when there are
+  // many chunks per position
+  int mt = 1;
+  while (mode == 0 && mt < 4 && n_chunks >= 8 * mt && threads * 2 <= 1024) {
+    mt <<= 1;
+    threads <<= 1;
+  }
   CanvasArgs a;
   a.B = p.batch;
   a.C = p.canvas_len;
@@ -263,6 +320,7 @@ cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Par
   a.st = st;
   a.part = part;
   a.n_chunks = n_chunks;
+  a.merge_threads = mt;
   a.mode = mode;
   a.row_mask = row_mask;
   canvas_step_kernel<<<p.batch, threads, 0, s>>>(a);

@@ -225,6 +225,23 @@ __device__ __forceinline__ void coop_eval(bool pass, const float (&z)[8], uint32
   for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
 }
 
+// Order-preserving map of floats to signed integers (for atomicMax).
+__device__ __forceinline__ int32_t f2ord(float f) {
+  const int32_t i = __float_as_int(f);
+  return i >= 0 ? i : (i ^ 0x7FFFFFFF);
+}
+__device__ __forceinline__ float ord2f(int32_t i) {
+  return __int_as_float(i >= 0 ? i : (i ^ 0x7FFFFFFF));
+}
+// The warps of a CTA that work on chunks of the same position share the best
+// attained score through shared memory: publish this warp's bound and take
+// the position's.
+__device__ __forceinline__ void share_bound(int32_t *slot, float &wb, int lane) {
+  int32_t v = 0;
+  if (lane == 0) v = atomicMax(slot, f2ord(wb));
+  wb = fmaxf(wb, ord2f(__shfl_sync(0xFFFFFFFFu, v, 0)));
+}
+
 // Careful path for any group (n <= 8 members, any values): flags NaN / +inf,
 // skips -inf, evaluates every finite member's Gumbel score exactly.
 __device__ void group_careful(const float *z, int n, uint32_t g, float c, const Keys &K, Lane &L,
@@ -345,14 +362,21 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
                       const uint8_t *__restrict__ phase, const uint64_t *__restrict__ request_id,
                       const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
                       Partial *__restrict__ part, uint32_t *__restrict__ status) {
+  __shared__ int32_t s_bound[kWarps];  // best score per position handled by this CTA
   const int lane = threadIdx.x & 31;
-  const int64_t wg = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int warp = threadIdx.x >> 5;
+  if (lane == 0) s_bound[warp] = f2ord(-INFINITY);
+  __syncthreads();
+  const int64_t wg = (int64_t)blockIdx.x * kWarps + warp;
   if (wg >= n_pos * (int64_t)n_chunks) return;
   const int64_t pos = wg / n_chunks;
   const int32_t ch = (int32_t)(wg - pos * n_chunks);
   const int64_t r = pos / C;
   const int64_t i = pos - r * C;
   if (phase[r] != DG_PHASE_DENOISE) return;
+  // slot of this position among the positions the CTA covers
+  const int64_t pos0 = ((int64_t)blockIdx.x * kWarps) / n_chunks;
+  int32_t *slot = &s_bound[(int)(pos - pos0)];
   Partial *out = part + wg;
 
   const float T = temperature[r];
@@ -416,6 +440,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
+      share_bound(slot, wb, lane);
     }
     for (int base = rounds * 128; base < n_full; base += 32) {
       const int q = base + lane;
@@ -451,6 +476,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         coop_eval(pass, z, g, h, c, wb, K, L, lane);
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
+      share_bound(slot, wb, lane);
     }
     for (int base = rounds * 64; base < n_full; base += 32) {
       const int q = base + lane;
@@ -479,6 +505,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       }
       coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
       if ((base & 511) == 480) fold_block(L); else if ((base & 127) == 96) fold_round(L);
+      if ((base & 127) == 96) share_bound(slot, wb, lane);
     }
   }
 

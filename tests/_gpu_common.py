@@ -17,7 +17,8 @@ from oracle import selfcond as osc
 
 ENT_TOL = 1e-4       # entropy, absolute (nats)
 M_TOL = 1e-4         # m = max z / T, absolute
-S_RTOL = 1e-5        # s, relative
+S_RTOL = 5e-5        # s, relative: every term of s uses the fast exp2 approximation; s
+                     # enters only ln s in the entropy (1e-4 budget) and the bf16 p rebuild
 SC_RTOL = 2e-2       # self-conditioning, relative (row norm and max-scaled elementwise)
 
 _POOL = None
@@ -116,8 +117,10 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
         v = valid
         assert np.all(np.abs(g["entropy"][sl][v] - ost.entropy[r][v]) <= ENT_TOL), (r, "entropy",
                np.max(np.abs(g["entropy"][sl][v] - ost.entropy[r][v])))
-        assert np.all(np.abs(g["m"][sl][v] - ost.m[r][v]) <= M_TOL), (r, "m")
-        assert np.all(np.abs(g["s"][sl][v] / ost.s[r][v] - 1.0) <= S_RTOL), (r, "s")
+        assert np.all(np.abs(g["m"][sl][v] - ost.m[r][v]) <= M_TOL), (
+            r, "m", float(np.max(np.abs(g["m"][sl][v] - ost.m[r][v]))))
+        rel = np.abs(g["s"][sl][v] / ost.s[r][v] - 1.0)
+        assert np.all(rel <= S_RTOL), (r, "s", float(rel.max()), int(np.argmax(rel)))
         assert np.array_equal(g["argmax"][sl], ost.argmax[r]), (r, "argmax")
         assert np.array_equal(g["argmax_prev"][sl], ost.argmax_prev[r]), (r, "argmax_prev")
         fc = flags.cand[r]
