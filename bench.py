@@ -188,6 +188,26 @@ def cpu_baseline_subprocess(wl_name: str, budget_s: float = 12.0):
     raise RuntimeError("cpu oracle leg failed: " + r.stderr[-2000:])
 
 
+# ------------------------------------------------------- multi-rank logic
+
+def shard_request_ids(batch: int, rank: int):
+    """Weak scaling: every rank owns its own `batch` requests (no collective on
+    the data path); request ids are disjoint across ranks."""
+    return list(range(rank * batch, (rank + 1) * batch))
+
+
+def aggregate(ms_local, world, positions_per_step, steps, dist=None, device=None):
+    """Max over ranks of the timed milliseconds (a list), then whole-job
+    throughput = world * positions * steps / max time."""
+    import torch
+    ms = list(ms_local)
+    if world > 1 and dist is not None:
+        t = torch.tensor(ms, dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = [float(x) for x in t]
+    return ms, world * positions_per_step * steps / (ms[0] / 1e3)
+
+
 # ---------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, dev):
@@ -218,7 +238,7 @@ def run_ours(args, rank, world, dev):
     st = dg.State(B, C, dev)
     st.phase.fill_(dg.DG_PHASE_DENOISE)
     st.temperature.fill_(T)
-    st.request_id.copy_(torch.arange(B, device=dev) + rank * B)
+    st.request_id.copy_(torch.tensor(shard_request_ids(B, rank), device=dev))
     ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device=dev)
     out = torch.empty((B * C, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -285,15 +305,11 @@ def run_ours(args, rank, world, dev):
         torch.cuda.synchronize(dev)
         ms_e2e = e0.elapsed_time(e1)
 
-    if world > 1:
-        tm = torch.tensor([ms, ms_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(tm[0]), float(tm[1])
-
+    n_pos = B * C
+    (ms, ms_e2e), value = aggregate([ms, ms_e2e], world, n_pos, K,
+                                     dist if world > 1 else None, dev)
     if rank != 0:
         return None
-    n_pos = B * C
-    value = world * n_pos * K / (ms / 1e3)
     e2e_value = world * n_pos * Ke / (ms_e2e / 1e3) if Ke else None
     hbm, bf16, src = peaks()
     flops = 2.0 * n_pos * V * d
