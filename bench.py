@@ -362,17 +362,17 @@ def run_ours(args, rank, world, dev):
 
 def _selfcond_splits(rows, V, d):
     # mirrors the library's split plan only to count launches (no effect on timing)
-    BM, BN, BK, SMS = 128, 512, 32, 152
+    BM, BN, BK, SMS = 256, 256, 32, 152
     m, n, k = -(-rows // BM), -(-d // BN), -(-V // BK)
-    halves = -(-d // 256)
-    tiles = m * n
+    cl = 2 if m >= 2 else 1
+    tiles = -(-m // cl) * cl * n
     best, best_eff = 1, 0.0
     for sp in range(1, 65):
         if sp > 1 and k // sp < 16:
             break
         ctas = tiles * sp
         waves = -(-ctas // SMS)
-        eff = m * halves * 0.5 * sp / (waves * SMS)
+        eff = m * n * sp / (waves * SMS)
         if eff > best_eff + 0.05:
             best, best_eff = sp, eff
     kbps = -(-k // best)

@@ -2,16 +2,16 @@
 // Blackwell tensor cores (Technical Report section 3.2, eq. 6: the p0 E inside
 // FFW(p0 E)).
 //
-// The probabilities are never stored: each 128 x 32 tile of bf16 logits
+// The probabilities are never stored: each 256 x 32 tile of bf16 logits
 // arrives by TMA in the 64-byte-swizzled K-major layout the MMA reads, and
 // eight producer warps turn it into p in place,
 // p = 2^(z*log2(e)/T - (m*log2(e) + log2 s)), from the per-position (m, s)
 // the sampler step wrote (fp32 or unaligned logits are loaded by the producers
-// instead).  The E tile (32 vocabulary rows x 512 embedding columns, bf16,
-// N-major, 128-byte swizzle) arrives by TMA.  One thread issues two
-// tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) per 16 vocabulary
-// rows into a 512-column TMEM accumulator, so every exponential feeds 512
-// columns of MMA work; the epilogue reads TMEM back with tcgen05.ld.
+// instead).  The E tile (32 vocabulary rows x 256 embedding columns, bf16,
+// N-major, 128-byte swizzle) arrives by TMA and serves two M=128 MMAs (the two
+// row halves), so each staged byte of E feeds 256 rows of work.  One thread
+// issues the tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into two
+// 256-column TMEM accumulators; the epilogue reads them back with tcgen05.ld.
 // Small batches split the vocabulary (K) across CTAs and reduce the fp32
 // partial sums in a second kernel.  Every wait is bounded: a wait that gives up
 // sets DG_DEV_WAIT_TIMEOUT, the CTA drains what it issued and returns.
@@ -27,16 +27,17 @@
 namespace dg {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 512;  // two N=256 MMAs per k-step
+constexpr int BM = 256;  // rows per CTA: two M=128 MMAs share every E tile
+constexpr int BN = 256;  // embedding columns per CTA (one N=256 MMA per row half)
 constexpr int BK = 32;   // one 64-byte swizzle row of bf16
-constexpr int NST = 5;
+constexpr int NST = 6;
 constexpr int kProdWarps = 8;
 constexpr int kThreads = 64 + 32 * kProdWarps;  // warp 0 TMA, warp 1 MMA, 8 producer/epilogue
-constexpr uint32_t kABytes = BM * BK * 2;  // 8 KB
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kAHalf = 128 * BK * 2;  // 8 KB: one M=128 operand
 constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 32 rows x 128 B
-constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
-constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + 2048 + 1024;
+constexpr uint32_t kBBytes = BK * BN * 2;  // 16 KB
+constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + 4096 + 1024;
 constexpr int kAssumedSMs = 152;
 #ifndef DG_WAIT_NS
 #define DG_WAIT_NS 2000000000ull
@@ -166,9 +167,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B N-major, M=128, N=256.
+// Instruction descriptor: bf16 x bf16 -> fp32, A K-major, B N-major, M=128, N=256
+// (each MMA covers one 128-row half of the CTA's 256 rows).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
-                            ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+                            ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
@@ -356,8 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t *sB = smem;                   // NST x 32 KB (1024-aligned)
-  uint8_t *sA = smem + NST * kBBytes;   // NST x 8 KB
+  uint8_t *sB = smem;                   // NST x 16 KB (1024-aligned)
+  uint8_t *sA = smem + NST * kBBytes;   // NST x 16 KB
   Shared *sh = reinterpret_cast<Shared *>(smem + NST * (kABytes + kBBytes));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -373,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb0 = split * a.kb_per_split;
   const int kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
   const int nkb = max(0, kb1 - kb0);
-  const int n_half = (n0 + 256 < a.d) ? 2 : 1;                    // MMAs per k-step
-  const int n_box = min(BN / 64, (a.d - n0 + 63) / 64);           // E boxes per stage
+  const int n_box = min(BN / 64, (a.d - n0 + 63) / 64);  // E boxes per stage
   const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes + (a.tma_a ? kABytes : 0u);
 
   if (threadIdx.x == 0) {
@@ -389,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->any_valid = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp >= 2 && threadIdx.x - 64 < BM) {
-    const int t = threadIdx.x - 64;
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;  // 0..255: one row each
     float c = 0.f, l2 = 0.f;
     const bool ok = row_feeds(a, row0 + t, c, l2);
     sh->row_c[t] = c;
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&sh->tmem_base)),
-                 "r"(BN));
+                 "r"(2 * BN));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -456,11 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_base = smem_u32(sB + s * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = smem_desc(a_base + kk * 32, 16, 512, 4);
-            for (int h = 0; h < n_half; ++h) {
-              const uint64_t bd =
-                  smem_desc(b_base + h * (4 * kBBoxBytes) + kk * 2048, kBBoxBytes, 1024, 2);
-              mma_bf16(tmem + (uint32_t)(h * 256), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = smem_desc(b_base + kk * 2048, kBBoxBytes, 1024, 2);
+#pragma unroll
+            for (int mh = 0; mh < 2; ++mh) {
+              const uint64_t ad = smem_desc(a_base + mh * kAHalf + kk * 32, 16, 512, 4);
+              mma_bf16(tmem + (uint32_t)(mh * BN), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
           if (CL == 1)
@@ -474,12 +475,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // ------------------------------------------------ p producers
       const int t = threadIdx.x - 64;  // 0..255
-      // two (row, 16-byte chunk) units per thread, fixed across stages
-      const int r0 = t >> 2, r1 = r0 + 64, ch = t & 3;
-      const float c0 = sh->row_c[r0], l0 = sh->row_l2[r0];
-      const float c1 = sh->row_c[r1], l1 = sh->row_l2[r1];
-      const bool ok0 = sh->row_ok[r0] != 0, ok1 = sh->row_ok[r1] != 0;
-      const uint32_t off0 = a_off(r0, ch), off1 = a_off(r1, ch);
+      // four (row, 16-byte chunk) units per thread, fixed across stages
+      const int ch = t & 3;
+      int rr[4];
+      float cc[4], ll[4];
+      bool okk[4];
+      uint32_t off[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        rr[j] = (t >> 2) + 64 * j;
+        cc[j] = sh->row_c[rr[j]];
+        ll[j] = sh->row_l2[rr[j]];
+        okk[j] = sh->row_ok[rr[j]] != 0;
+        off[j] = a_off(rr[j], ch);
+      }
       if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -491,28 +500,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t *tileA = sA + s * kABytes;
           const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
           const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
-          uint4 *u0 = reinterpret_cast<uint4 *>(tileA + off0);
-          uint4 *u1 = reinterpret_cast<uint4 *>(tileA + off1);
-          const uint4 v0 = *u0, v1 = *u1;
-          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-          *u0 = ok0 ? p_from_bf16(w0, c0, l0, valid) : make_uint4(0u, 0u, 0u, 0u);
-          *u1 = ok1 ? p_from_bf16(w1, c1, l1, valid) : make_uint4(0u, 0u, 0u, 0u);
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tileA + off[j]);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            *reinterpret_cast<uint4 *>(tileA + off[j]) =
+                okk[j] ? p_from_bf16(w, cc[j], ll[j], valid) : make_uint4(0u, 0u, 0u, 0u);
+          }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
         }
       } else {
         const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
-        const char *rp0 =
-            reinterpret_cast<const char *>(a.logits) + (size_t)(row0 + r0) * (size_t)a.ld * esz;
-        const char *rp1 =
-            reinterpret_cast<const char *>(a.logits) + (size_t)(row0 + r1) * (size_t)a.ld * esz;
-        Raw8 x0, x1;
+        const char *rp[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          rp[j] = reinterpret_cast<const char *>(a.logits) +
+                  (size_t)(row0 + rr[j]) * (size_t)a.ld * esz;
+        Raw8 x[4];
         if (nkb > 0) {
           const int64_t k = (int64_t)kb0 * BK + ch * 8;
-          if (ok0) x0 = load_raw8(a, rp0, k);
-          if (ok1) x1 = load_raw8(a, rp1, k);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (okk[j]) x[j] = load_raw8(a, rp[j], k);
         }
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -525,23 +538,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
           const int64_t rem = (int64_t)a.V - k;
           const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
-          uint4 p0 = make_uint4(0u, 0u, 0u, 0u), p1 = p0;
-          if (a.dtype == DG_BF16) {
-            const uint32_t w0[4] = {x0.w[0], x0.w[1], x0.w[2], x0.w[3]};
-            const uint32_t w1[4] = {x1.w[0], x1.w[1], x1.w[2], x1.w[3]};
-            if (ok0) p0 = p_from_bf16(w0, c0, l0, valid);
-            if (ok1) p1 = p_from_bf16(w1, c1, l1, valid);
-          } else {
-            if (ok0) p0 = p_from_f32(x0.w, c0, l0, valid);
-            if (ok1) p1 = p_from_f32(x1.w, c1, l1, valid);
+          uint4 pv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            pv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (okk[j]) {
+              if (a.dtype == DG_BF16) {
+                const uint32_t w[4] = {x[j].w[0], x[j].w[1], x[j].w[2], x[j].w[3]};
+                pv[j] = p_from_bf16(w, cc[j], ll[j], valid);
+              } else {
+                pv[j] = p_from_f32(x[j].w, cc[j], ll[j], valid);
+              }
+            }
           }
           // prefetch the next stage's logits while this one is consumed
           if (i + 1 < nkb) {
-            if (ok0) x0 = load_raw8(a, rp0, k + BK);
-            if (ok1) x1 = load_raw8(a, rp1, k + BK);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (okk[j]) x[j] = load_raw8(a, rp[j], k + BK);
           }
-          *reinterpret_cast<uint4 *>(tileA + off0) = p0;
-          *reinterpret_cast<uint4 *>(tileA + off1) = p1;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(tileA + off[j]) = pv[j];
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
@@ -552,21 +569,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------- epilogue
   if (warp >= 2) {
-    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;         // which 256 accumulator columns
-    const int r = quarter * 32 + lane;
+    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+    const int mh = (warp - 2) >> 2;      // which 128-row half (and accumulator)
+    const int r = mh * 128 + quarter * 32 + lane;
     const int64_t q = row0 + r;
     bool have = false;
     if (run) have = mbar_wait(&sh->tmem_full, 0, sh, a.status, where_code(3, 3, 0, 0));
     have = __all_sync(0xFFFFFFFFu, have);
     tc_fence_after();
     const bool ok = have && sh->row_ok[r] != 0;
-    for (int cb = half * 256; cb < half * 256 + 256; cb += 32) {
+    for (int cb = 0; cb < BN; cb += 32) {
       const int col0 = n0 + cb;
       if (col0 >= a.d) break;  // warp-uniform
       float v[32];
       if (have) {
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cb, v);
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(mh * BN + cb), v);
       }
       // per-lane conditions guard only the stores, never the warp-wide TMEM loads
       const int ncol = min(32, a.d - col0);
@@ -603,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN));
   }
   // no CTA leaves while a peer may still signal its barriers or write its
   // shared memory
@@ -674,8 +691,6 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
   pl.cluster = pl.m_tiles >= 2 ? 2 : 1;
   pl.m_groups = (pl.m_tiles + pl.cluster - 1) / pl.cluster;
   const int64_t m_pad = (int64_t)pl.m_groups * pl.cluster;
-  // work units in half tiles (the last column tile may be half wide)
-  const int64_t halves_per_m = (d + 255) / 256;
   const int64_t tiles = m_pad * pl.n_tiles;
   // Choose the split count whose CTA count fills the SMs best (waves of
   // kAssumedSMs), keeping at least 16 k-blocks per split.
@@ -685,7 +700,7 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
     if (sp > 1 && pl.k_blocks / sp < 16) break;
     const int64_t ctas = tiles * sp;
     const int64_t waves = (ctas + kAssumedSMs - 1) / kAssumedSMs;
-    const double work = (double)pl.m_tiles * (double)halves_per_m * 0.5 * sp;
+    const double work = (double)pl.m_tiles * (double)pl.n_tiles * sp;
     const double eff = work / (double)(waves * kAssumedSMs);
     if (eff > best_eff + 0.05) {
       best_eff = eff;
@@ -755,7 +770,7 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   if (tma_a) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.vocab, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.logits_ld * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};  // 32 columns x 256 rows
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(logits), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
