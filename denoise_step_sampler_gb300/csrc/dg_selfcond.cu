@@ -332,6 +332,19 @@ __device__ __forceinline__ uint4 p_from_bf16(const uint32_t (&w)[4], float c, fl
   return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                     pack_bf16x2(p[6], p[7]));
 }
+// Same as p_from_bf16 for a chunk wholly inside the vocabulary (no bounds
+// checks), with the exponent arguments formed by packed f32x2 FMAs.
+__device__ __forceinline__ uint4 p_from_bf16_full(const uint4 &v, uint64_t cc, uint64_t nl) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t out[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint64_t z = pack2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+    const uint64_t arg = fma2(z, cc, nl);
+    out[j] = pack_bf16x2(ex2_approx(lo2(arg)), ex2_approx(hi2(arg)));
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
 __device__ __forceinline__ uint4 p_from_f32(const uint32_t (&w)[8], float c, float l2,
                                             int valid) {
   float p[8];
@@ -482,12 +495,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool okk[4];
       uint32_t off[4];
 #pragma unroll
+      uint64_t cc2[4], nl2[4];
       for (int j = 0; j < 4; ++j) {
         rr[j] = (t >> 2) + 64 * j;
         cc[j] = sh->row_c[rr[j]];
         ll[j] = sh->row_l2[rr[j]];
         okk[j] = sh->row_ok[rr[j]] != 0;
         off[j] = a_off(rr[j], ch);
+        cc2[j] = pack2(cc[j], cc[j]);
+        nl2[j] = pack2(-ll[j], -ll[j]);
       }
       if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
@@ -498,16 +514,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                           mbar_wait(&sh->full[s], par, sh, a.status, where_code(2, 0, s, i))))
             break;
           uint8_t *tileA = sA + s * kABytes;
-          const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
-          const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
           uint4 v[4];
 #pragma unroll
           for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tileA + off[j]);
+          if ((int64_t)(kb0 + i + 1) * BK <= (int64_t)a.V) {  // warp-uniform: block inside V
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-            *reinterpret_cast<uint4 *>(tileA + off[j]) =
-                okk[j] ? p_from_bf16(w, cc[j], ll[j], valid) : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4 *>(tileA + off[j]) =
+                  okk[j] ? p_from_bf16_full(v[j], cc2[j], nl2[j]) : make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
+            const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+              *reinterpret_cast<uint4 *>(tileA + off[j]) =
+                  okk[j] ? p_from_bf16(w, cc[j], ll[j], valid) : make_uint4(0u, 0u, 0u, 0u);
+            }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
