@@ -172,57 +172,80 @@ __device__ __forceinline__ bool group8(const float (&z)[8], uint32_t g, float c,
   return w <= thr * 1.001f;
 }
 
-// Warp-cooperative exact evaluation of the groups that passed the screen
-// (one flag per lane, all 32 lanes call this).  Up to four passing groups
-// are evaluated at a time, eight lanes per group and one member per lane, so
-// the rare exact draws run convergently instead of one lane at a time.  Each
-// evaluating lane keeps the best (score, index) it saw; the warp merge at the
-// end takes the overall maximum, lowest index on ties.  The warp-wide bound
-// wb is refreshed afterwards.
-__device__ __forceinline__ void coop_eval(bool pass, const float (&z)[8], uint32_t g, uint32_t h,
-                                          float c, float &wb, const Keys &K, Lane &L, int lane) {
-  uint32_t mask = __ballot_sync(0xFFFFFFFFu, pass);
-  if (mask == 0u) return;
+// Exact evaluation of the groups that passed the screen, deferred through a
+// per-warp queue in shared memory so that it always runs in full batches:
+// four queued groups at a time, eight lanes per group and one member per
+// lane, so the rare exact draws run convergently and no batch is mostly idle.
+// Each evaluating lane keeps the best (score, index) it saw; the warp merge at
+// the end takes the overall maximum, lowest index on ties.  Groups are
+// screened against the bound known when they were queued and evaluated
+// against the (tighter) bound known when their batch runs; both are scores
+// some member of the position attains, so no possible winner is skipped.
+struct QEntry {
+  float z[8];
+  uint32_t g, h, pad0, pad1;
+};
+constexpr int kQueue = 64;  // entries per warp (at most 3 + 32 are ever pending)
+
+struct Queue {
+  QEntry *q;  // this warp's ring
+  int head, count;  // warp-uniform
+};
+
+__device__ __forceinline__ void run_batch(Queue &Q, int cnt, float c, float &wb, const Keys &K,
+                                          Lane &L, int lane) {
   const int slot = lane >> 3, j = lane & 7;
   const float sb = wb;
-  while (mask != 0u) {
-    uint32_t mm = mask;
-    int owner = -1;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int bit = mm ? (__ffs(mm) - 1) : -1;
-      if (k == slot) owner = bit;
-      if (mm) mm &= mm - 1u;
-    }
-    mask = mm;
-    const int src = owner >= 0 ? owner : lane;
-    float zj = 0.f;
-#pragma unroll
-    for (int jj = 0; jj < 8; ++jj) {
-      const float v = __shfl_sync(0xFFFFFFFFu, z[jj], src);
-      if (jj == j) zj = v;
-    }
-    const uint32_t gg = __shfl_sync(0xFFFFFFFFu, g, src);
-    const uint32_t hh = __shfl_sync(0xFFFFFFFFu, h, src);
-    if (owner >= 0) {
-      const float base = exp1_draw(hh) * 0.125f;
-      // E_j >= X/8, so score_j <= z_j c - log2(X/8): skip if below sb
-      if (!(base > ex2_approx(fmaf(zj, c, -sb)) * 1.001f)) {
-        const uint32_t J = below(fmix32(K.kb ^ gg), 8u);
-        float E = base;
-        if ((uint32_t)j != J) E += exp1_draw(fmix32(K.kc ^ (gg * kGroup + (uint32_t)j)));
-        const float sc = fmaf(zj, c, -__log2f(E));
-        const int32_t idx = (int32_t)(gg * kGroup + (uint32_t)j);
-        if (sc > L.b2 || (sc == L.b2 && (uint32_t)idx < (uint32_t)L.cand)) {
-          L.b2 = sc;
-          L.cand = idx;
-        }
+  if (slot < cnt) {
+    const QEntry &e = Q.q[(Q.head + slot) & (kQueue - 1)];
+    const float zj = e.z[j];
+    const uint32_t gg = e.g, hh = e.h;
+    const float base = exp1_draw(hh) * 0.125f;
+    // E_j >= X/8, so score_j <= z_j c - log2(X/8): skip if below sb
+    if (!(base > ex2_approx(fmaf(zj, c, -sb)) * 1.001f)) {
+      const uint32_t J = below(fmix32(K.kb ^ gg), 8u);
+      float E = base;
+      if ((uint32_t)j != J) E += exp1_draw(fmix32(K.kc ^ (gg * kGroup + (uint32_t)j)));
+      const float sc = fmaf(zj, c, -__log2f(E));
+      const int32_t idx = (int32_t)(gg * kGroup + (uint32_t)j);
+      if (sc > L.b2 || (sc == L.b2 && (uint32_t)idx < (uint32_t)L.cand)) {
+        L.b2 = sc;
+        L.cand = idx;
       }
     }
   }
+  Q.head = (Q.head + cnt) & (kQueue - 1);
+  Q.count -= cnt;
   wb = fmaxf(wb, L.b2);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
+}
+
+// All 32 lanes call this after screening one group each.
+__device__ __forceinline__ void coop_eval(bool pass, const float (&z)[8], uint32_t g, uint32_t h,
+                                          float c, float &wb, const Keys &K, Lane &L, int lane,
+                                          Queue &Q) {
+  const uint32_t mask = __ballot_sync(0xFFFFFFFFu, pass);
+  if (mask == 0u) return;
+  if (pass) {
+    const int pos = Q.head + Q.count + __popc(mask & ((1u << lane) - 1u));
+    QEntry &e = Q.q[pos & (kQueue - 1)];
+    *reinterpret_cast<float4 *>(&e.z[0]) = make_float4(z[0], z[1], z[2], z[3]);
+    *reinterpret_cast<float4 *>(&e.z[4]) = make_float4(z[4], z[5], z[6], z[7]);
+    e.g = g;
+    e.h = h;
+  }
+  Q.count += __popc(mask);
+  __syncwarp();
+  while (Q.count >= 4) run_batch(Q, 4, c, wb, K, L, lane);
+  __syncwarp();
+}
+
+__device__ __forceinline__ void flush_queue(Queue &Q, float c, float &wb, const Keys &K, Lane &L,
+                                            int lane) {
+  __syncwarp();
+  while (Q.count > 0) run_batch(Q, Q.count < 4 ? Q.count : 4, c, wb, K, L, lane);
+  __syncwarp();
 }
 
 // Order-preserving map of floats to signed integers (for atomicMax).
@@ -363,6 +386,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
                       const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
                       Partial *__restrict__ part, uint32_t *__restrict__ status) {
   __shared__ int32_t s_bound[kWarps];  // best score per position handled by this CTA
+  __shared__ QEntry s_queue[kWarps][kQueue];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if (lane == 0) s_bound[warp] = f2ord(-INFINITY);
@@ -422,6 +446,10 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   // predicated per lane), so the warp-cooperative steps are reached by all 32
   // lanes.
   float wb = -INFINITY;  // best score attained anywhere in the warp so far
+  Queue Q;
+  Q.q = &s_queue[threadIdx.x >> 5][0];
+  Q.head = 0;
+  Q.count = 0;
   if (aligned && DT == DG_BF16) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
     const int rounds = n_full / 128;
@@ -437,7 +465,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         const uint32_t g = g0 + (uint32_t)(q + u * 32);
         uint32_t h;
         const bool pass = group8(z, g, c, wb, K, L, h);
-        coop_eval(pass, z, g, h, c, wb, K, L, lane);
+        coop_eval(pass, z, g, h, c, wb, K, L, lane, Q);
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
@@ -451,7 +479,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         unpack_bf16x8(ld_stream(vrow + q), z);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
     }
   } else if (aligned) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
@@ -473,7 +501,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         const uint32_t g = g0 + (uint32_t)(q + u * 32);
         uint32_t h;
         const bool pass = group8(z, g, c, wb, K, L, h);
-        coop_eval(pass, z, g, h, c, wb, K, L, lane);
+        coop_eval(pass, z, g, h, c, wb, K, L, lane, Q);
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
@@ -491,7 +519,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
     }
   } else {
     for (int base = 0; base < n_full; base += 32) {  // warp-uniform trip count
@@ -503,12 +531,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
         load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane);
+      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
       if ((base & 511) == 480) fold_block(L); else if ((base & 127) == 96) fold_round(L);
       if ((base & 127) == 96) share_bound(slot, wb, lane);
     }
   }
 
+  flush_queue(Q, c, wb, K, L, lane);
   float s, t;
   sums(L, s, t);
   const bool bad = !(isfinite(s) && isfinite(t));
