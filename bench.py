@@ -46,18 +46,22 @@ METRIC = "denoise-step positions/s (sampler+self-cond)"
 SEED = 0xD1FF0002
 
 
-def traffic_for(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary of a kernel, only if
-    the kernel's source is unchanged since the capture (else None)."""
+def traffic_for(call: str, workload: str):
+    """DRAM bytes per call (all of its kernels) from the committed ncu summary,
+    only for the profiled workload and only while every source file of the
+    call is unchanged since the capture (else None)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            table = json.load(f)
-        ent = table[kernel_file]
-        src = os.path.join(ROOT, "denoise_step_sampler_gb300", "csrc", kernel_file)
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return ent["dram_bytes_per_launch"] if ent.get("source_sha256_16") == h else None
-    except Exception:
+            ent = json.load(f)[call]
+        if ent["workload"] != workload:
+            return None
+        for name, want in ent["sources"].items():
+            src = os.path.join(ROOT, "denoise_step_sampler_gb300", "csrc", name)
+            if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != want:
+                return None
+        return ent["dram_bytes_per_call"]
+    except (OSError, KeyError, ValueError):
         return None
 
 
@@ -167,8 +171,13 @@ def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None =
         osc.selfcond_rows(zrows.astype(np.float64), Tf, E)
         return time.perf_counter() - t0
 
+    # t(P) = fixed + P * per_position (the fp64 E read is the fixed part): size
+    # the sample from two probes so that the timed run takes about budget_s
     t1 = run(z)
-    P = max(1, int(budget_s / max(t1, 1e-3)))
+    z8 = syn.boosted_logits(8, V, seed=SEED, dtype=tdt, device="cpu", boost_hi=boost).float().numpy()
+    t8 = run(z8)
+    per = max((t8 - t1) / 7.0, 1e-4)
+    P = max(1, int((budget_s - max(t1 - per, 0.0)) / per))
     if max_positions:
         P = min(P, max_positions)
     z = syn.boosted_logits(P, V, seed=SEED, dtype=tdt, device="cpu", boost_hi=boost).float().numpy()
@@ -353,13 +362,13 @@ def run_ours(args, rank, world, dev):
         "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16,
-                     "traffic": traffic_for("dg_selfcond.cu") if args.workload == DEFAULT and not args.batch else None,
+                     "traffic": None if args.batch else traffic_for("dg_selfcond_embed", args.workload),
                      "peak_source": f"{src} bf16 burst", "flops_per_launch": flops,
                      "ms_per_launch": ms_sc},
         "roofline_sampler": {"bound": "hbm", "kernel": "dg_denoise_step (vocab pass + canvas step)",
                              "achieved": sampler_gbs, "peak": hbm, "unit": "GB/s",
                              "frac": sampler_gbs / hbm,
-                             "traffic": traffic_for("dg_vocab.cu") if args.workload == DEFAULT and not args.batch else None,
+                             "traffic": None if args.batch else traffic_for("dg_denoise_step", args.workload),
                              "peak_source": f"{src} copy", "bytes_per_launch": logit_bytes,
                              "ms_per_launch": ms_sampler},
         "clocks": clk,
@@ -382,7 +391,7 @@ def run_ours(args, rank, world, dev):
 
 def _selfcond_splits(rows, V, d):
     # mirrors the library's split plan only to count launches (no effect on timing)
-    BM, BN, BK, SMS = 256, 256, 32, 152
+    BM, BN, BK, SMS = 256, 256, 64, 152
     m, n, k = -(-rows // BM), -(-d // BN), -(-V // BK)
     cl = 2 if m >= 2 else 1
     tiles = -(-m // cl) * cl * n

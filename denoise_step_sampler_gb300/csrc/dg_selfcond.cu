@@ -2,14 +2,17 @@
 // Blackwell tensor cores (Technical Report section 3.2, eq. 6: the p0 E inside
 // FFW(p0 E)).
 //
-// The probabilities are never stored: each 256 x 32 tile of bf16 logits
-// arrives by TMA in the 64-byte-swizzled K-major layout the MMA reads, and
+// The probabilities are never stored: each 256 x 64 tile of bf16 logits
+// arrives by TMA in the 128-byte-swizzled K-major layout the MMA reads, and
 // eight producer warps turn it into p in place,
 // p = 2^(z*log2(e)/T - (m*log2(e) + log2 s)), from the per-position (m, s)
 // the sampler step wrote (fp32 or unaligned logits are loaded by the producers
-// instead).  The E tile (32 vocabulary rows x 256 embedding columns, bf16,
+// instead).  The E tile (64 vocabulary rows x 256 embedding columns, bf16,
 // N-major, 128-byte swizzle) arrives by TMA and serves two M=128 MMAs (the two
-// row halves), so each staged byte of E feeds 256 rows of work.  One thread
+// row halves), so each staged byte of E feeds 256 rows of work.  A tiled TMA
+// copy holds the thread that issues it for a time that grows with the box's
+// row count, so tiles are 128 bytes wide (half the rows per byte of 64-byte
+// tiles) and are issued by four warps: two for the logits halves, two for E.  One thread
 // issues the tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32) into two
 // 256-column TMEM accumulators; the epilogue reads them back with tcgen05.ld.
 // Small batches split the vocabulary (K) across CTAs and reduce the fp32
@@ -29,15 +32,22 @@ namespace {
 
 constexpr int BM = 256;  // rows per CTA: two M=128 MMAs share every E tile
 constexpr int BN = 256;  // embedding columns per CTA (one N=256 MMA per row half)
-constexpr int BK = 32;   // one 64-byte swizzle row of bf16
-constexpr int NST = 6;
+constexpr int BK = 64;   // one 128-byte swizzle row of bf16
+constexpr int NST = 3;   // stages of 64 KB
 constexpr int kProdWarps = 8;
-constexpr int kThreads = 64 + 32 * kProdWarps;  // warp 0 TMA, warp 1 MMA, 8 producer/epilogue
-constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
-constexpr uint32_t kAHalf = 128 * BK * 2;  // 8 KB: one M=128 operand
-constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 32 rows x 128 B
-constexpr uint32_t kBBytes = BK * BN * 2;  // 16 KB
-constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + 4096 + 1024;
+constexpr int kAIssuers = 2;  // logits-tile TMA warps (one 128-row half each)
+constexpr int kFirstAWarp = 2 + kProdWarps;
+constexpr int kSecondEWarp = kFirstAWarp + kAIssuers;
+// warp 0 E-tile TMA, warp 1 MMA, 8 producer/epilogue warps, 2 logits-tile TMA,
+// 1 more E-tile TMA
+constexpr int kThreads = 32 * (kSecondEWarp + 1);
+constexpr uint32_t kABytes = BM * BK * 2;  // 32 KB
+constexpr uint32_t kAHalf = 128 * BK * 2;  // 16 KB: one M=128 operand
+constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 64 rows x 128 B
+constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
+constexpr uint32_t kSharedBytes = 1024;  // barriers + per-row flags, after the stages
+constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + kSharedBytes + 1024;  // + alignment
+static_assert(kSmemBytes <= 232448, "over the 227 KB per-CTA shared memory limit");
 constexpr int kAssumedSMs = 152;
 #ifndef DG_WAIT_NS
 #define DG_WAIT_NS 2000000000ull
@@ -46,7 +56,8 @@ constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
 
 template <int NS>
 struct SharedT {
-  uint64_t full[NS];     // TMA bytes of the stage landed
+  uint64_t full[NS];     // TMA bytes of the stage's E tile landed
+  uint64_t a_full[NS];   // TMA bytes of the stage's logits tile landed
   uint64_t a_ready[NS];  // producers wrote p into the A tile
   uint64_t empty[NS];    // the MMAs reading the stage completed
   uint64_t tmem_full;
@@ -54,11 +65,10 @@ struct SharedT {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t any_valid;
-  float row_c[BM];
-  float row_l2[BM];
-  int32_t row_ok[BM];
+  uint8_t row_ok[BM];
 };
 using Shared = SharedT<NST>;
+static_assert(sizeof(Shared) <= kSharedBytes, "barrier block outgrew its reservation");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -355,10 +365,10 @@ __device__ __forceinline__ uint4 p_from_f32(const uint32_t (&w)[8], float c, flo
                     pack_bf16x2(p[6], p[7]));
 }
 
-// Byte offset of 16-byte chunk `ch` (0..3) of row `r` in a 64-byte-swizzled
-// K-major tile (8-row atoms of 512 bytes).
+// Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
+// K-major tile (8-row atoms of 1024 bytes).
 __device__ __forceinline__ uint32_t a_off(int r, int ch) {
-  return (uint32_t)(r * 64 + ((ch ^ ((r >> 1) & 3)) << 4));
+  return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
 // CL CTAs form a cluster over CL consecutive row tiles of one column tile and
@@ -389,11 +399,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
   const int nkb = max(0, kb1 - kb0);
   const int n_box = min(BN / 64, (a.d - n0 + 63) / 64);  // E boxes per stage
-  const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes + (a.tma_a ? kABytes : 0u);
+  const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes;  // E bytes landing in this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->a_full[s], kAIssuers);
       mbar_init(&sh->a_ready[s], kProdWarps);
       mbar_init(&sh->empty[s], CL);  // one MMA-commit arrival from each CTA of the cluster
     }
@@ -403,12 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->any_valid = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp >= 2) {
+  if (warp >= 2 && warp < kFirstAWarp) {
     const int t = threadIdx.x - 64;  // 0..255: one row each
-    float c = 0.f, l2 = 0.f;
+    float c, l2;
     const bool ok = row_feeds(a, row0 + t, c, l2);
-    sh->row_c[t] = c;
-    sh->row_l2[t] = l2;
     sh->row_ok[t] = ok ? 1 : 0;
     if (ok) atomicOr(&sh->any_valid, 1);
   }
@@ -430,9 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool run = any != 0 && nkb > 0;
 
   if (run) {
-    if (warp == 0) {
-      // ------------------------------------------------ TMA producer
-      if (lane == 0) {
+    if (warp == 0 || warp == kSecondEWarp) {
+      // ------------------------------------------------ E-tile TMA
+      // This CTA loads the boxes j with j % CL == rank (multicast to the
+      // cluster when CL > 1); the two E warps take alternate ones.  Warp 0
+      // alone posts the stage's expected bytes (all boxes, own and peers').
+      const int e = (warp == 0) ? 0 : 1;
+      int mine = 0;
+      for (int j = rank; j < n_box; j += CL) mine += ((j / CL) & 1) == e;
+      if (lane == 0 && (mine > 0 || e == 0)) {
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -440,17 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i >= NST &&
               !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
             break;
-          mbar_expect_tx(&sh->full[s], stage_tx);
+          if (e == 0) mbar_expect_tx(&sh->full[s], stage_tx);
           const int32_t kv = (kb0 + i) * BK;
           uint8_t *dstB = sB + s * kBBytes;
-          for (int j = 0; j < n_box; ++j) {
+          for (int j = rank; j < n_box; j += CL) {
+            if (((j / CL) & 1) != e) continue;
             if (CL == 1)
               tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
-            else if (j % CL == rank)
+            else
               tma_load_2d_mc(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv,
                              cl_mask);
           }
-          if (a.tma_a) tma_load_2d(sA + s * kABytes, &tmap_z, &sh->full[s], kv, (int32_t)row0);
           issued = i + 1;
         }
         // every issued copy must land before the CTA may exit
@@ -473,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = smem_desc(b_base + kk * 2048, kBBoxBytes, 1024, 2);
 #pragma unroll
             for (int mh = 0; mh < 2; ++mh) {
-              const uint64_t ad = smem_desc(a_base + mh * kAHalf + kk * 32, 16, 512, 4);
+              const uint64_t ad = smem_desc(a_base + mh * kAHalf + kk * 32, 16, 1024, 2);
               mma_bf16(tmem + (uint32_t)(mh * BN), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
@@ -485,25 +500,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&sh->tmem_full);
         mma_commit(&sh->mma_done);
       }
+    } else if (warp >= kFirstAWarp) {  // (kSecondEWarp is taken above)
+      // ------------------------------------------------ logits-tile TMA (one 128-row half each)
+      const int h = warp - kFirstAWarp;
+      if (lane == 0 && a.tma_a) {
+        int issued = 0;
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NST;
+          const uint32_t use = (uint32_t)(i / NST);
+          if (i >= NST &&
+              !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(4, 2, s, i)))
+            break;
+          mbar_expect_tx(&sh->a_full[s], kAHalf);
+          tma_load_2d(sA + s * kABytes + h * kAHalf, &tmap_z, &sh->a_full[s], (kb0 + i) * BK,
+                      (int32_t)(row0 + h * 128));
+          issued = i + 1;
+        }
+        // every issued copy must land before the CTA may exit
+        for (int i = max(0, issued - NST); i < issued; ++i)
+          mbar_drain(&sh->a_full[i % NST], (uint32_t)(i / NST) & 1u);
+      }
     } else {
       // ------------------------------------------------ p producers
       const int t = threadIdx.x - 64;  // 0..255
-      // four (row, 16-byte chunk) units per thread, fixed across stages
-      const int ch = t & 3;
-      int rr[4];
-      float cc[4], ll[4];
-      bool okk[4];
-      uint32_t off[4];
+      // Eight (row, 16-byte chunk) units per thread, fixed across stages:
+      // unit j is row (t >> 3) + 32 j, chunk t & 7, so each unit index of a
+      // warp covers four whole 128-byte rows (no bank conflicts).
+      const int ch = t & 7;
+      uint32_t okm = 0;  // bit j: the row of unit j feeds the next step
+      uint64_t cc2[8], nl2[8];
 #pragma unroll
-      uint64_t cc2[4], nl2[4];
-      for (int j = 0; j < 4; ++j) {
-        rr[j] = (t >> 2) + 64 * j;
-        cc[j] = sh->row_c[rr[j]];
-        ll[j] = sh->row_l2[rr[j]];
-        okk[j] = sh->row_ok[rr[j]] != 0;
-        off[j] = a_off(rr[j], ch);
-        cc2[j] = pack2(cc[j], cc[j]);
-        nl2[j] = pack2(-ll[j], -ll[j]);
+      for (int j = 0; j < 8; ++j) {
+        float c = 0.f, l2 = 0.f;
+        if (row_feeds(a, row0 + (t >> 3) + 32 * j, c, l2)) okm |= 1u << j;
+        cc2[j] = pack2(c, c);
+        nl2[j] = pack2(-l2, -l2);
       }
       if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
@@ -511,25 +542,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t par = (uint32_t)(i / NST) & 1u;
           // the whole warp leaves together if the wait gives up
           if (!__all_sync(0xFFFFFFFFu,
-                          mbar_wait(&sh->full[s], par, sh, a.status, where_code(2, 0, s, i))))
+                          mbar_wait(&sh->a_full[s], par, sh, a.status, where_code(2, 4, s, i))))
             break;
           uint8_t *tileA = sA + s * kABytes;
-          uint4 v[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tileA + off[j]);
           if ((int64_t)(kb0 + i + 1) * BK <= (int64_t)a.V) {  // warp-uniform: block inside V
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4 *>(tileA + off[j]) =
-                  okk[j] ? p_from_bf16_full(v[j], cc2[j], nl2[j]) : make_uint4(0u, 0u, 0u, 0u);
+            for (int hh = 0; hh < 2; ++hh) {  // two passes of four units
+              uint4 v[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj)
+                v[jj] = *reinterpret_cast<const uint4 *>(
+                    tileA + a_off((t >> 3) + 32 * (4 * hh + jj), ch));
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const int j = 4 * hh + jj;
+                *reinterpret_cast<uint4 *>(tileA + a_off((t >> 3) + 32 * j, ch)) =
+                    ((okm >> j) & 1u) ? p_from_bf16_full(v[jj], cc2[j], nl2[j])
+                                      : make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
           } else {
             const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
             const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-              *reinterpret_cast<uint4 *>(tileA + off[j]) =
-                  okk[j] ? p_from_bf16(w, cc[j], ll[j], valid) : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < 8; ++j) {
+              uint8_t *u = tileA + a_off((t >> 3) + 32 * j, ch);
+              const uint4 v = *reinterpret_cast<const uint4 *>(u);
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              *reinterpret_cast<uint4 *>(u) =
+                  ((okm >> j) & 1u) ? p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid)
+                                    : make_uint4(0u, 0u, 0u, 0u);
             }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -537,19 +579,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
         }
       } else {
+        // The producers load the logits themselves: each stage in two
+        // sub-steps of four units, each sub-step prefetching the next.
         const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
-        const char *rp[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          rp[j] = reinterpret_cast<const char *>(a.logits) +
-                  (size_t)(row0 + rr[j]) * (size_t)a.ld * esz;
+        const char *rowp = reinterpret_cast<const char *>(a.logits) +
+                           (size_t)(row0 + (t >> 3)) * (size_t)a.ld * esz;
+        const size_t jstride = (size_t)32 * (size_t)a.ld * esz;  // unit j's row: rowp + j * jstride
         Raw8 x[4];
-        if (nkb > 0) {
-          const int64_t k = (int64_t)kb0 * BK + ch * 8;
+        auto load4 = [&](int i, int hh) {
+          const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (okk[j]) x[j] = load_raw8(a, rp[j], k);
-        }
+          for (int jj = 0; jj < 4; ++jj) {
+            const int j = 4 * hh + jj;
+            if ((okm >> j) & 1u) x[jj] = load_raw8(a, rowp + (size_t)j * jstride, k);
+          }
+        };
+        if (nkb > 0) load4(0, 0);
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
           const uint32_t use = (uint32_t)(i / NST);
@@ -561,27 +606,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
           const int64_t rem = (int64_t)a.V - k;
           const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
-          uint4 pv[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            pv[j] = make_uint4(0u, 0u, 0u, 0u);
-            if (okk[j]) {
-              if (a.dtype == DG_BF16) {
-                const uint32_t w[4] = {x[j].w[0], x[j].w[1], x[j].w[2], x[j].w[3]};
-                pv[j] = p_from_bf16(w, cc[j], ll[j], valid);
-              } else {
-                pv[j] = p_from_f32(x[j].w, cc[j], ll[j], valid);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint4 pv[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int j = 4 * hh + jj;
+              pv[jj] = make_uint4(0u, 0u, 0u, 0u);
+              if ((okm >> j) & 1u) {
+                if (a.dtype == DG_BF16) {
+                  const uint32_t w[4] = {x[jj].w[0], x[jj].w[1], x[jj].w[2], x[jj].w[3]};
+                  pv[jj] = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                } else {
+                  pv[jj] = p_from_f32(x[jj].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                }
               }
             }
-          }
-          // prefetch the next stage's logits while this one is consumed
-          if (i + 1 < nkb) {
+            if (hh == 0)
+              load4(i, 1);
+            else if (i + 1 < nkb)
+              load4(i + 1, 0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (okk[j]) x[j] = load_raw8(a, rp[j], k + BK);
+            for (int jj = 0; jj < 4; ++jj)
+              *reinterpret_cast<uint4 *>(tileA + a_off((t >> 3) + 32 * (4 * hh + jj), ch)) = pv[jj];
           }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(tileA + off[j]) = pv[j];
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
@@ -591,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---------------------------------------------------- epilogue
-  if (warp >= 2) {
+  if (warp >= 2 && warp < kFirstAWarp) {
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
     const int mh = (warp - 2) >> 2;      // which 128-row half (and accumulator)
     const int r = mh * 128 + quarter * 32 + lane;
@@ -793,10 +841,10 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   if (tma_a) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.vocab, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)p.logits_ld * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};  // 32 columns x 256 rows
+    const cuuint32_t box[2] = {(cuuint32_t)BK, 128u};  // 64 columns x 128 rows (half a tile)
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(logits), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
