@@ -34,13 +34,13 @@ constexpr int BM = 256;  // rows per CTA: two M=128 MMAs share every E tile
 constexpr int BN = 256;  // embedding columns per CTA (one N=256 MMA per row half)
 constexpr int BK = 64;   // one 128-byte swizzle row of bf16
 constexpr int NST = 3;   // stages of 64 KB
-constexpr int kProdWarps = 8;
-constexpr int kAIssuers = 2;  // logits-tile TMA warps (one 128-row half each)
+constexpr int kProdWarps = 16;  // four per scheduler: the p rebuild is latency-bound
+constexpr int kAIssuers = 2;  // TMA warps that also load one 128-row half of the logits tile
 constexpr int kFirstAWarp = 2 + kProdWarps;
-constexpr int kSecondEWarp = kFirstAWarp + kAIssuers;
-// warp 0 E-tile TMA, warp 1 MMA, 8 producer/epilogue warps, 2 logits-tile TMA,
-// 1 more E-tile TMA
-constexpr int kThreads = 32 * (kSecondEWarp + 1);
+// warp 0 E-tile TMA, warp 1 MMA, 16 producer/epilogue warps, 2 logits-and-E
+// TMA warps (20 warps: a multiple of 4, so the register cap is 96)
+constexpr int kThreads = 32 * (kFirstAWarp + kAIssuers);
+constexpr int kTmaWarps = 1 + kAIssuers;  // E boxes are dealt round-robin over these
 constexpr uint32_t kABytes = BM * BK * 2;  // 32 KB
 constexpr uint32_t kAHalf = 128 * BK * 2;  // 16 KB: one M=128 operand
 constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 64 rows x 128 B
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh->any_valid = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp >= 2 && warp < kFirstAWarp) {
+  if (warp >= 2 && threadIdx.x - 64 < BM) {
     const int t = threadIdx.x - 64;  // 0..255: one row each
     float c, l2;
     const bool ok = row_feeds(a, row0 + t, c, l2);
@@ -439,15 +439,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool run = any != 0 && nkb > 0;
 
   if (run) {
-    if (warp == 0 || warp == kSecondEWarp) {
-      // ------------------------------------------------ E-tile TMA
-      // This CTA loads the boxes j with j % CL == rank (multicast to the
-      // cluster when CL > 1); the two E warps take alternate ones.  Warp 0
-      // alone posts the stage's expected bytes (all boxes, own and peers').
-      const int e = (warp == 0) ? 0 : 1;
+    if (warp == 0 || warp >= kFirstAWarp) {
+      // ------------------------------------------------ TMA
+      // TMA warp tw (0: warp 0; 1, 2: the logits warps) loads the logits half
+      // tw - 1 (tw >= 1) and the E boxes j with j % CL == rank (multicast to
+      // the cluster when CL > 1) whose index among this CTA's boxes is tw
+      // modulo kTmaWarps.  Warp 0 alone posts the stage's expected E bytes
+      // (all boxes, own and peers').
+      const int tw = (warp == 0) ? 0 : 1 + (warp - kFirstAWarp);
+      const bool do_a = a.tma_a && tw >= 1;
       int mine = 0;
-      for (int j = rank; j < n_box; j += CL) mine += ((j / CL) & 1) == e;
-      if (lane == 0 && (mine > 0 || e == 0)) {
+      for (int j = rank; j < n_box; j += CL) mine += ((j / CL) % kTmaWarps) == tw;
+      if (lane == 0 && (do_a || mine > 0 || tw == 0)) {
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -455,11 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i >= NST &&
               !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
             break;
-          if (e == 0) mbar_expect_tx(&sh->full[s], stage_tx);
           const int32_t kv = (kb0 + i) * BK;
+          if (do_a) {
+            mbar_expect_tx(&sh->a_full[s], kAHalf);
+            tma_load_2d(sA + s * kABytes + (tw - 1) * kAHalf, &tmap_z, &sh->a_full[s], kv,
+                        (int32_t)(row0 + (tw - 1) * 128));
+          }
+          if (tw == 0) mbar_expect_tx(&sh->full[s], stage_tx);
           uint8_t *dstB = sB + s * kBBytes;
           for (int j = rank; j < n_box; j += CL) {
-            if (((j / CL) & 1) != e) continue;
+            if (((j / CL) % kTmaWarps) != tw) continue;
             if (CL == 1)
               tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
             else
@@ -469,8 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = i + 1;
         }
         // every issued copy must land before the CTA may exit
-        for (int i = max(0, issued - NST); i < issued; ++i)
+        for (int i = max(0, issued - NST); i < issued; ++i) {
           mbar_drain(&sh->full[i % NST], (uint32_t)(i / NST) & 1u);
+          if (do_a) mbar_drain(&sh->a_full[i % NST], (uint32_t)(i / NST) & 1u);
+        }
       }
     } else if (warp == 1) {
       // ------------------------------------------------ MMA issuer
@@ -500,42 +510,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&sh->tmem_full);
         mma_commit(&sh->mma_done);
       }
-    } else if (warp >= kFirstAWarp) {  // (kSecondEWarp is taken above)
-      // ------------------------------------------------ logits-tile TMA (one 128-row half each)
-      const int h = warp - kFirstAWarp;
-      if (lane == 0 && a.tma_a) {
-        int issued = 0;
-        for (int i = 0; i < nkb; ++i) {
-          const int s = i % NST;
-          const uint32_t use = (uint32_t)(i / NST);
-          if (i >= NST &&
-              !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(4, 2, s, i)))
-            break;
-          mbar_expect_tx(&sh->a_full[s], kAHalf);
-          tma_load_2d(sA + s * kABytes + h * kAHalf, &tmap_z, &sh->a_full[s], (kb0 + i) * BK,
-                      (int32_t)(row0 + h * 128));
-          issued = i + 1;
-        }
-        // every issued copy must land before the CTA may exit
-        for (int i = max(0, issued - NST); i < issued; ++i)
-          mbar_drain(&sh->a_full[i % NST], (uint32_t)(i / NST) & 1u);
-      }
     } else {
       // ------------------------------------------------ p producers
-      const int t = threadIdx.x - 64;  // 0..255
-      // Eight (row, 16-byte chunk) units per thread, fixed across stages:
-      // unit j is row (t >> 3) + 32 j, chunk t & 7, so each unit index of a
+      const int t = threadIdx.x - 64;  // 0..511
+      // Four (row, 16-byte chunk) units per thread, fixed across stages:
+      // unit j is row (t >> 3) + 64 j, chunk t & 7, so each unit index of a
       // warp covers four whole 128-byte rows (no bank conflicts).
       const int ch = t & 7;
       uint32_t okm = 0;  // bit j: the row of unit j feeds the next step
-      uint64_t cc2[8], nl2[8];
+      uint64_t cc2[4], nl2[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         float c = 0.f, l2 = 0.f;
-        if (row_feeds(a, row0 + (t >> 3) + 32 * j, c, l2)) okm |= 1u << j;
+        if (row_feeds(a, row0 + (t >> 3) + 64 * j, c, l2)) okm |= 1u << j;
         cc2[j] = pack2(c, c);
         nl2[j] = pack2(-l2, -l2);
       }
+      uint32_t off[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) off[j] = a_off((t >> 3) + 64 * j, ch);
       if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -545,31 +538,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                           mbar_wait(&sh->a_full[s], par, sh, a.status, where_code(2, 4, s, i))))
             break;
           uint8_t *tileA = sA + s * kABytes;
+          uint4 v[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tileA + off[j]);
           if ((int64_t)(kb0 + i + 1) * BK <= (int64_t)a.V) {  // warp-uniform: block inside V
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {  // two passes of four units
-              uint4 v[4];
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj)
-                v[jj] = *reinterpret_cast<const uint4 *>(
-                    tileA + a_off((t >> 3) + 32 * (4 * hh + jj), ch));
-#pragma unroll
-              for (int jj = 0; jj < 4; ++jj) {
-                const int j = 4 * hh + jj;
-                *reinterpret_cast<uint4 *>(tileA + a_off((t >> 3) + 32 * j, ch)) =
-                    ((okm >> j) & 1u) ? p_from_bf16_full(v[jj], cc2[j], nl2[j])
-                                      : make_uint4(0u, 0u, 0u, 0u);
-              }
-            }
+            for (int j = 0; j < 4; ++j)
+              *reinterpret_cast<uint4 *>(tileA + off[j]) =
+                  ((okm >> j) & 1u) ? p_from_bf16_full(v[j], cc2[j], nl2[j])
+                                    : make_uint4(0u, 0u, 0u, 0u);
           } else {
             const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
             const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              uint8_t *u = tileA + a_off((t >> 3) + 32 * j, ch);
-              const uint4 v = *reinterpret_cast<const uint4 *>(u);
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-              *reinterpret_cast<uint4 *>(u) =
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+              *reinterpret_cast<uint4 *>(tileA + off[j]) =
                   ((okm >> j) & 1u) ? p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid)
                                     : make_uint4(0u, 0u, 0u, 0u);
             }
@@ -579,22 +563,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
         }
       } else {
-        // The producers load the logits themselves: each stage in two
-        // sub-steps of four units, each sub-step prefetching the next.
+        // The producers load the logits themselves, one stage ahead.
         const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
         const char *rowp = reinterpret_cast<const char *>(a.logits) +
                            (size_t)(row0 + (t >> 3)) * (size_t)a.ld * esz;
-        const size_t jstride = (size_t)32 * (size_t)a.ld * esz;  // unit j's row: rowp + j * jstride
+        const size_t jstride = (size_t)64 * (size_t)a.ld * esz;  // unit j's row: rowp + j * jstride
         Raw8 x[4];
-        auto load4 = [&](int i, int hh) {
-          const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
+        if (nkb > 0) {
+          const int64_t k = (int64_t)kb0 * BK + ch * 8;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * hh + jj;
-            if ((okm >> j) & 1u) x[jj] = load_raw8(a, rowp + (size_t)j * jstride, k);
-          }
-        };
-        if (nkb > 0) load4(0, 0);
+          for (int j = 0; j < 4; ++j)
+            if ((okm >> j) & 1u) x[j] = load_raw8(a, rowp + (size_t)j * jstride, k);
+        }
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
           const uint32_t use = (uint32_t)(i / NST);
@@ -606,30 +586,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;
           const int64_t rem = (int64_t)a.V - k;
           const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
+          uint4 pv[4];
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint4 pv[4];
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-              const int j = 4 * hh + jj;
-              pv[jj] = make_uint4(0u, 0u, 0u, 0u);
-              if ((okm >> j) & 1u) {
-                if (a.dtype == DG_BF16) {
-                  const uint32_t w[4] = {x[jj].w[0], x[jj].w[1], x[jj].w[2], x[jj].w[3]};
-                  pv[jj] = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
-                } else {
-                  pv[jj] = p_from_f32(x[jj].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
-                }
+          for (int j = 0; j < 4; ++j) {
+            pv[j] = make_uint4(0u, 0u, 0u, 0u);
+            if ((okm >> j) & 1u) {
+              if (a.dtype == DG_BF16) {
+                const uint32_t w[4] = {x[j].w[0], x[j].w[1], x[j].w[2], x[j].w[3]};
+                pv[j] = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+              } else {
+                pv[j] = p_from_f32(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               }
             }
-            if (hh == 0)
-              load4(i, 1);
-            else if (i + 1 < nkb)
-              load4(i + 1, 0);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj)
-              *reinterpret_cast<uint4 *>(tileA + a_off((t >> 3) + 32 * (4 * hh + jj), ch)) = pv[jj];
           }
+          // prefetch the next stage's logits while this one is consumed
+          if (i + 1 < nkb) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if ((okm >> j) & 1u) x[j] = load_raw8(a, rowp + (size_t)j * jstride, k + BK);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(tileA + off[j]) = pv[j];
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->a_ready[s]);
@@ -640,8 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------------------------------------------- epilogue
   if (warp >= 2 && warp < kFirstAWarp) {
+    const int ew = warp - 2;             // 0..15
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
-    const int mh = (warp - 2) >> 2;      // which 128-row half (and accumulator)
+    const int mh = (ew >> 2) & 1;        // which 128-row half (and accumulator)
+    const int cbase = (ew >> 3) * (BN / 2);  // which half of the columns
     const int r = mh * 128 + quarter * 32 + lane;
     const int64_t q = row0 + r;
     bool have = false;
@@ -649,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     have = __all_sync(0xFFFFFFFFu, have);
     tc_fence_after();
     const bool ok = have && sh->row_ok[r] != 0;
-    for (int cb = 0; cb < BN; cb += 32) {
+    for (int cb = cbase; cb < cbase + BN / 2; cb += 32) {
       const int col0 = n0 + cb;
       if (col0 >= a.d) break;  // warp-uniform
       float v[32];
