@@ -49,6 +49,10 @@ constexpr uint32_t kSharedBytes = 1024;  // barriers + per-row flags, after the 
 constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + kSharedBytes + 1024;  // + alignment
 static_assert(kSmemBytes <= 232448, "over the 227 KB per-CTA shared memory limit");
 constexpr int kAssumedSMs = 152;
+// E tiles come mostly from DRAM, logits tiles mostly from L2 (the column tiles
+// of a row block run side by side), so one CTA per cluster asks L2 for the E
+// tile this many k-blocks before it is loaded.
+constexpr int kPrefetchKb = 4;
 #ifndef DG_WAIT_NS
 #define DG_WAIT_NS 2000000000ull
 #endif
@@ -155,6 +159,12 @@ __device__ __noinline__ void mbar_drain(uint64_t *b, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int32_t x, int32_t y) {
   asm volatile(
@@ -377,7 +387,8 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
 template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
-                         const __grid_constant__ CUtensorMap tmap_z, GemmArgs a) {
+                         const __grid_constant__ CUtensorMap tmap_z,
+                         const __grid_constant__ CUtensorMap tmap_ep, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -450,7 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool do_a = a.tma_a && tw >= 1;
       int mine = 0;
       for (int j = rank; j < n_box; j += CL) mine += ((j / CL) % kTmaWarps) == tw;
+      const bool prefetch = tw == 0 && rank == 0;
       if (lane == 0 && (do_a || mine > 0 || tw == 0)) {
+        if (prefetch)
+          for (int i = 0; i < min(kPrefetchKb, nkb); ++i)
+            tma_prefetch_2d(&tmap_ep, n0, (kb0 + i) * BK);
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NST;
@@ -474,6 +489,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d_mc(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv,
                              cl_mask);
           }
+          if (prefetch && i + kPrefetchKb < nkb)
+            tma_prefetch_2d(&tmap_ep, n0, (kb0 + i + kPrefetchKb) * BK);
           issued = i + 1;
         }
         // every issued copy must land before the CTA may exit
@@ -766,8 +783,9 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
 
 namespace {
 template <int CL>
-cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z, const GemmArgs &a,
-                        int64_t grid, cudaStream_t s) {
+cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
+                        const CUtensorMap &map_ep, const GemmArgs &a, int64_t grid,
+                        cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -791,7 +809,7 @@ cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z, cons
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL>, map_e, map_z, a);
+  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL>, map_e, map_z, map_ep, a);
 }
 
 }  // namespace
@@ -802,7 +820,7 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int64_t rows = (int64_t)p.batch * p.canvas_len;
-  CUtensorMap map_e, map_z;
+  CUtensorMap map_e, map_z, map_ep;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
     const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
@@ -810,6 +828,17 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(E), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    // the same E, one 256-column x BK-row box per k-block, for L2 prefetches only
+    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BN, (cuuint32_t)BK};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map_ep, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(E), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -856,9 +885,9 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   const int64_t grid = (int64_t)plan.m_groups * plan.cluster * plan.n_tiles * plan.splits;
   cudaError_t e;
   if (plan.cluster == 2)
-    e = launch_gemm<2>(map_e, map_z, a, grid, s);
+    e = launch_gemm<2>(map_e, map_z, map_ep, a, grid, s);
   else
-    e = launch_gemm<1>(map_e, map_z, a, grid, s);
+    e = launch_gemm<1>(map_e, map_z, map_ep, a, grid, s);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
