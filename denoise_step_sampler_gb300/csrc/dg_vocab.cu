@@ -30,12 +30,17 @@ struct Keys {
 // The softmax sums are kept in three levels so that no fp32 sum adds more
 // than a few dozen terms: S/T collect one round of groups, BS/BT collect up
 // to 16 rounds, ts/tt the rest of the chunk.
+//
+// The sums are taken relative to a reference m2 (base 2), any value at or
+// below the running maximum of z c: with a = z c - m2, s = sum 2^a and
+// t = sum a 2^a give the same entropy log2 s - t/s for every choice of m2,
+// and the reference only keeps the terms in range.
 struct Lane {
   float zmax;   // running max of stored logits
-  int32_t am;   // its lowest index
-  float m2;     // fl(zmax * c)
-  uint64_t S0, S1, T0, T1;      // packed round sums of 2^a and a 2^a
-  uint64_t BS, BT;              // packed block sums
+  int32_t am;   // its lowest index (-1 until known)
+  float m2;     // reference of the sums (-inf while they are empty)
+  float2 S0, S1, T0, T1;        // round sums of 2^a and a 2^a, in pairs
+  float2 BS, BT;                // block sums
   float ts, tt;                 // chunk totals
   float b2;     // best perturbed score, base 2
   int32_t cand;
@@ -45,8 +50,8 @@ __device__ __forceinline__ void lane_init(Lane &L) {
   L.zmax = -INFINITY;
   L.am = -1;
   L.m2 = -INFINITY;
-  L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
-  L.BS = L.BT = 0ull;
+  L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
+  L.BS = L.BT = make_float2(0.f, 0.f);
   L.ts = L.tt = 0.f;
   L.b2 = -INFINITY;
   L.cand = -1;
@@ -54,16 +59,16 @@ __device__ __forceinline__ void lane_init(Lane &L) {
 
 // Round sums into the block sums.
 __device__ __forceinline__ void fold_round(Lane &L) {
-  L.BS = add2(L.BS, add2(L.S0, L.S1));
-  L.BT = add2(L.BT, add2(L.T0, L.T1));
-  L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
+  L.BS = __fadd2_rn(L.BS, __fadd2_rn(L.S0, L.S1));
+  L.BT = __fadd2_rn(L.BT, __fadd2_rn(L.T0, L.T1));
+  L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
 }
 // Block sums into the chunk totals.
 __device__ __forceinline__ void fold_block(Lane &L) {
   fold_round(L);
-  L.ts += lo2(L.BS) + hi2(L.BS);
-  L.tt += lo2(L.BT) + hi2(L.BT);
-  L.BS = L.BT = 0ull;
+  L.ts += L.BS.x + L.BS.y;
+  L.tt += L.BT.x + L.BT.y;
+  L.BS = L.BT = make_float2(0.f, 0.f);
 }
 
 __device__ __forceinline__ void sums(Lane &L, float &s, float &t) {
@@ -72,29 +77,30 @@ __device__ __forceinline__ void sums(Lane &L, float &s, float &t) {
   t = L.tt;
 }
 
-// The running maximum moved from L.m2 to m2n: rescale the sums of every
-// level (s' = s 2^d, t' = (t + d s) 2^d with d = m2 - m2n <= 0).
+// Move the reference of the sums from L.m2 up to m2n: rescale every level
+// (s' = s 2^d, t' = (t + d s) 2^d with d = m2 - m2n <= 0).
 __device__ __forceinline__ void rescale(Lane &L, float m2n) {
-  if (L.zmax == -INFINITY) {
-    L.S0 = L.S1 = L.T0 = L.T1 = 0ull;
-    L.BS = L.BT = 0ull;
+  if (L.m2 == -INFINITY) {
+    L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
+    L.BS = L.BT = make_float2(0.f, 0.f);
     L.ts = L.tt = 0.f;
+    L.m2 = m2n;
     return;
   }
   const float d = L.m2 - m2n;
   const float f = ex2_approx(d);
-  auto one = [&](uint64_t &S, uint64_t &T) {
-    float s0 = lo2(S), s1 = hi2(S), t0 = lo2(T), t1 = hi2(T);
-    t0 = fmaf(d, s0, t0) * f;
-    t1 = fmaf(d, s1, t1) * f;
-    S = pack2(s0 * f, s1 * f);
-    T = pack2(t0, t1);
+  auto one = [&](float2 &S, float2 &T) {
+    T.x = fmaf(d, S.x, T.x) * f;
+    T.y = fmaf(d, S.y, T.y) * f;
+    S.x *= f;
+    S.y *= f;
   };
   one(L.S0, L.T0);
   one(L.S1, L.T1);
   one(L.BS, L.BT);
   L.tt = fmaf(d, L.ts, L.tt) * f;
   L.ts *= f;
+  L.m2 = m2n;
 }
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -146,25 +152,25 @@ __device__ __forceinline__ bool group8(const float (&z)[8], uint32_t g, float c,
     L.am = (int32_t)(g * kGroup + j);
     L.m2 = m2n;
   }
-  const uint64_t cc = pack2(c, c);
-  const uint64_t mm = pack2(-L.m2, -L.m2);
+  const float2 cc = make_float2(c, c);
+  const float2 mm = make_float2(-L.m2, -L.m2);
   {
-    const uint64_t a0 = fma2(pack2(z[0], z[1]), cc, mm);
-    const uint64_t a1 = fma2(pack2(z[2], z[3]), cc, mm);
-    const uint64_t a2 = fma2(pack2(z[4], z[5]), cc, mm);
-    const uint64_t a3 = fma2(pack2(z[6], z[7]), cc, mm);
-    const uint64_t e0 = pack2(ex2_approx(lo2(a0)), ex2_approx(hi2(a0)));
-    const uint64_t e1 = pack2(ex2_approx(lo2(a1)), ex2_approx(hi2(a1)));
-    const uint64_t e2 = pack2(ex2_approx(lo2(a2)), ex2_approx(hi2(a2)));
-    const uint64_t e3 = pack2(ex2_approx(lo2(a3)), ex2_approx(hi2(a3)));
-    L.S0 = add2(L.S0, e0);
-    L.S1 = add2(L.S1, e1);
-    L.T0 = fma2(a0, e0, L.T0);
-    L.T1 = fma2(a1, e1, L.T1);
-    L.S0 = add2(L.S0, e2);
-    L.S1 = add2(L.S1, e3);
-    L.T0 = fma2(a2, e2, L.T0);
-    L.T1 = fma2(a3, e3, L.T1);
+    const float2 a0 = __ffma2_rn(make_float2(z[0], z[1]), cc, mm);
+    const float2 a1 = __ffma2_rn(make_float2(z[2], z[3]), cc, mm);
+    const float2 a2 = __ffma2_rn(make_float2(z[4], z[5]), cc, mm);
+    const float2 a3 = __ffma2_rn(make_float2(z[6], z[7]), cc, mm);
+    const float2 e0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+    const float2 e1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
+    const float2 e2 = make_float2(ex2_approx(a2.x), ex2_approx(a2.y));
+    const float2 e3 = make_float2(ex2_approx(a3.x), ex2_approx(a3.y));
+    L.S0 = __fadd2_rn(L.S0, e0);
+    L.S1 = __fadd2_rn(L.S1, e1);
+    L.T0 = __ffma2_rn(a0, e0, L.T0);
+    L.T1 = __ffma2_rn(a1, e1, L.T1);
+    L.S0 = __fadd2_rn(L.S0, e2);
+    L.S1 = __fadd2_rn(L.S1, e3);
+    L.T0 = __ffma2_rn(a2, e2, L.T0);
+    L.T1 = __ffma2_rn(a3, e3, L.T1);
   }
   h = fmix32(K.ka ^ g);
   const float w = (float)(~h) * 2.3283064365386963e-10f;
@@ -303,11 +309,36 @@ __device__ void group_careful(const float *z, int n, uint32_t g, float c, const 
     s += e;
     t = fmaf(a, e, t);
   }
-  L.S0 = add2(L.S0, pack2(s, 0.f));
-  L.T0 = add2(L.T0, pack2(t, 0.f));
+  L.S0.x += s;
+  L.T0.x += t;
   if ((g & 15u) == 15u) fold_block(L); else fold_round(L);
   gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, L.b2, K, L);
 }
+
+// Largest of the 32 bf16 values of a round (NaN values are ignored; the sums
+// catch them).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162 *>(&a);
+  __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162 *>(&b);
+  __nv_bfloat162 r = __hmax2(x, y);
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ float round_max_bf16(const uint4 (&v)[4]) {
+  uint32_t m[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) m[u] = bmax2(bmax2(v[u].x, v[u].y), bmax2(v[u].z, v[u].w));
+  const uint32_t r = bmax2(bmax2(m[0], m[1]), bmax2(m[2], m[3]));
+  return fmaxf(__uint_as_float(r << 16), __uint_as_float(r & 0xFFFF0000u));
+}
+// float -> uint32, truncating, saturating (NaN -> 0).
+__device__ __forceinline__ uint32_t f2u_sat(float x) {
+  uint32_t r;
+  asm("cvt.rzi.sat.u32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// The sums' reference moves only when the maximum of z c passes it by more
+// than this (terms stay below 2^32, sums below 2^50).
+constexpr float kLazyRef = 32.f;
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&z)[8]) {
   z[0] = __uint_as_float(v.x << 16);
@@ -335,11 +366,14 @@ __device__ __forceinline__ void load_group_scalar(const void *row, int64_t v, in
   for (int j = 0; j < n; ++j) z[j] = load_scalar<DT>(row, v + j);
 }
 
-// Merge the 32 lanes' records; every lane ends with the warp result.
-__device__ __forceinline__ void warp_merge(float c, float &zmax, int32_t &am, float &s, float &t,
-                                           float &b2, int32_t &cand) {
+// Merge the 32 lanes' records; every lane ends with the warp result, its sums
+// relative to fl(zmax c).  Each lane's sums come relative to its own
+// reference m2.
+__device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32_t &am, float &s,
+                                           float &t, float &b2, int32_t &cand) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
+    const float om2 = __shfl_xor_sync(0xFFFFFFFFu, m2, off);
     const float oz = __shfl_xor_sync(0xFFFFFFFFu, zmax, off);
     const int32_t oam = __shfl_xor_sync(0xFFFFFFFFu, am, off);
     const float os = __shfl_xor_sync(0xFFFFFFFFu, s, off);
@@ -352,19 +386,20 @@ __device__ __forceinline__ void warp_merge(float c, float &zmax, int32_t &am, fl
       const float M2 = nz * c;
       float ns = 0.f, nt = 0.f;
       if (s > 0.f) {
-        const float d = zmax * c - M2;
+        const float d = m2 - M2;
         const float f = ex2_approx(d);
         ns += s * f;
         nt += fmaf(d, s, t) * f;
       }
       if (os > 0.f) {
-        const float d = oz * c - M2;
+        const float d = om2 - M2;
         const float f = ex2_approx(d);
         ns += os * f;
         nt += fmaf(d, os, ot) * f;
       }
       s = ns;
       t = nt;
+      m2 = M2;
     }
     if (oz > zmax || (oz == zmax && oam >= 0 && (am < 0 || oam < am))) {
       zmax = oz;
@@ -453,22 +488,76 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   if (aligned && DT == DG_BF16) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
     const int rounds = n_full / 128;
+    // Per round each lane holds 4 groups (32 logits).  The round's maximum
+    // (a packed bf16 max) serves three things at once: the running maximum
+    // (whose index is found once, at the end, from the round that set it),
+    // the reference of the sums (moved only when the maximum passes it by
+    // more than kLazyRef), and one Gumbel screening threshold for all four
+    // groups.
+    const float2 cc = make_float2(c, c);
+    int am_round = -1;
     for (int rd = 0; rd < rounds; ++rd) {
       const int q = rd * 128 + lane;
       uint4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) v[u] = ld_stream(vrow + q + u * 32);
+      const float rmax = round_max_bf16(v);
+      if (rmax > L.zmax) am_round = rd;
+      L.zmax = fmaxf(L.zmax, rmax);
+      const float m2r = rmax * c;
+      if (m2r > L.m2 + kLazyRef) rescale(L, m2r);  // the first finite round sets it
+      const float2 mm = make_float2(-L.m2, -L.m2);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        float z[8];
-        unpack_bf16x8(v[u], z);
-        const uint32_t g = g0 + (uint32_t)(q + u * 32);
-        uint32_t h;
-        const bool pass = group8(z, g, c, wb, K, L, h);
-        coop_eval(pass, z, g, h, c, wb, K, L, lane, Q);
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 a = __ffma2_rn(
+              make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)), cc, mm);
+          const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          if (k & 1) {
+            L.S1 = __fadd2_rn(L.S1, e);
+            L.T1 = __ffma2_rn(a, e, L.T1);
+          } else {
+            L.S0 = __fadd2_rn(L.S0, e);
+            L.T0 = __ffma2_rn(a, e, L.T0);
+          }
+        }
+      }
+      // Gumbel screen: group g can hold a score >= wb only if its W_g
+      // (= (~h + 1/2) 2^-32) <= 8 2^(vmax c - wb); with the round maximum for
+      // vmax and a 0.1 % margin that is ~h <= 2^(rmax c - wb + 35.00144).
+      const uint32_t lim = ~f2u_sat(ex2_approx(fmaf(rmax, c, -wb) + 35.0014415f));
+      uint32_t pm = 0;  // bit u: group u passes
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        pm |= (fmix32(K.ka ^ (g0 + (uint32_t)(q + u * 32))) >= lim ? 1u : 0u) << u;
+      if (__any_sync(0xFFFFFFFFu, pm != 0u)) {
+        // rare: reload the round (L2) and queue the passing groups
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t g = g0 + (uint32_t)(q + u * 32);
+          float z[8];
+          unpack_bf16x8(ld_stream(vrow + q + u * 32), z);
+          coop_eval((pm >> u) & 1u, z, g, fmix32(K.ka ^ g), c, wb, K, L, lane, Q);
+        }
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
+    }
+    if (am_round >= 0) {
+      // lowest index holding the lane's maximum, in the round that set it
+      const int q = am_round * 128 + lane;
+      int32_t best = -1;
+#pragma unroll
+      for (int u = 3; u >= 0; --u) {
+        float z[8];
+        unpack_bf16x8(ld_stream(vrow + q + u * 32), z);
+#pragma unroll
+        for (int j = 7; j >= 0; --j)
+          if (z[j] == L.zmax) best = (int32_t)((g0 + (uint32_t)(q + u * 32)) * kGroup + j);
+      }
+      L.am = best;
     }
     for (int base = rounds * 128; base < n_full; base += 32) {
       const int q = base + lane;
@@ -559,7 +648,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 
   float zmax = L.zmax, b2 = L.b2;
   int32_t am = L.am, cand = L.cand;
-  warp_merge(c, zmax, am, s, t, b2, cand);
+  warp_merge(c, L.m2, zmax, am, s, t, b2, cand);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, off);
   if (lane == 0) {
