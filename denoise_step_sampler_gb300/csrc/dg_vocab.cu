@@ -198,6 +198,18 @@ struct Queue {
   int head, count;  // warp-uniform
 };
 
+// Exact perturbed score (base 2) of member j of the full group g, with the
+// same operations as the batched evaluation below (so equal members score
+// equally wherever they are evaluated).
+__device__ __forceinline__ float exact_score8(float zj, uint32_t g, uint32_t j, float c,
+                                              const Keys &K) {
+  const float base = exp1_draw(fmix32(K.ka ^ g)) * 0.125f;
+  const uint32_t J = below(fmix32(K.kb ^ g), 8u);
+  float E = base;
+  if (j != J) E += exp1_draw(fmix32(K.kc ^ (g * kGroup + j)));
+  return fmaf(zj, c, -__log2f(E));
+}
+
 __device__ __forceinline__ void run_batch(Queue &Q, int cnt, float c, float &wb, const Keys &K,
                                           Lane &L, int lane) {
   const int slot = lane >> 3, j = lane & 7;
@@ -496,6 +508,36 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     // groups.
     const float2 cc = make_float2(c, c);
     int am_round = -1;
+    if (rounds > 0) {
+      // Warm start: each lane scores the largest logit of its first round
+      // exactly, so that the first round is already screened against a
+      // finite bound instead of queueing every group.
+      float zb = -INFINITY;
+      uint32_t ib = 0;
+#pragma unroll
+      for (int u = 3; u >= 0; --u) {
+        float z[8];
+        unpack_bf16x8(ld_stream(vrow + lane + u * 32), z);
+#pragma unroll
+        for (int j = 7; j >= 0; --j)
+          if (z[j] >= zb) {
+            zb = z[j];
+            ib = (uint32_t)(u * 8 + j);
+          }
+      }
+      if (zb > -INFINITY && zb < INFINITY) {  // NaN/inf chunks take the careful path anyway
+        const uint32_t g = g0 + (uint32_t)lane + (ib >> 3) * 32u;
+        const float sc = exact_score8(zb, g, ib & 7u, c, K);
+        if (sc > L.b2) {
+          L.b2 = sc;
+          L.cand = (int32_t)(g * kGroup + (ib & 7u));
+        }
+      }
+      wb = L.b2;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
+      share_bound(slot, wb, lane);
+    }
     for (int rd = 0; rd < rounds; ++rd) {
       const int q = rd * 128 + lane;
       uint4 v[4];
@@ -528,18 +570,19 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       // (= (~h + 1/2) 2^-32) <= 8 2^(vmax c - wb); with the round maximum for
       // vmax and a 0.1 % margin that is ~h <= 2^(rmax c - wb + 35.00144).
       const uint32_t lim = ~f2u_sat(ex2_approx(fmaf(rmax, c, -wb) + 35.0014415f));
-      uint32_t pm = 0;  // bit u: group u passes
+      const uint32_t gq = g0 + (uint32_t)q;
+      bool any = false;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        pm |= (fmix32(K.ka ^ (g0 + (uint32_t)(q + u * 32))) >= lim ? 1u : 0u) << u;
-      if (__any_sync(0xFFFFFFFFu, pm != 0u)) {
+      for (int u = 0; u < 4; ++u) any |= fmix32(K.ka ^ (gq + 32u * u)) >= lim;
+      if (__any_sync(0xFFFFFFFFu, any)) {
         // rare: reload the round (L2) and queue the passing groups
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint32_t g = g0 + (uint32_t)(q + u * 32);
+          const uint32_t g = gq + 32u * u;
+          const uint32_t h = fmix32(K.ka ^ g);
           float z[8];
           unpack_bf16x8(ld_stream(vrow + q + u * 32), z);
-          coop_eval((pm >> u) & 1u, z, g, fmix32(K.ka ^ g), c, wb, K, L, lane, Q);
+          coop_eval(h >= lim, z, g, h, c, wb, K, L, lane, Q);
         }
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
