@@ -158,3 +158,23 @@ def test_multistep_loop_until_every_request_commits():
             break
         denoise_and_compare(p, st, logits.reshape(-1))
     assert committed.all()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_large_logit_jumps_move_the_sum_reference(T):
+    """Spikes far above the running maximum (more than 2^32 in base 2) at early,
+    middle and late vocabulary indices force the vocabulary pass to move the
+    reference of its softmax sums mid-chunk; the results must still match."""
+    B, C, V = 1, 16, 262144
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=99,
+                  entropy_budget=8.0, conf_threshold=0.3, stable_k=3, step_cap=32)
+    logits = _logits(B, C, V, dg.DG_BF16, seed=7).view(B, C, V)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    for i in range(C):
+        n = 1 + i % 3
+        idx = torch.randint(0, V, (n,), generator=g).sort().values
+        for k, v in enumerate(idx.tolist()):
+            logits[0, i, v] = 20.0 + 30.0 * k + float(i)   # rising spikes
+    st = make_state(p, [dg.DG_PHASE_DENOISE], request_ids=[3], temperatures=[T])
+    denoise_and_compare(p, st, logits.reshape(-1))
