@@ -23,8 +23,8 @@ DiffusionGemmaModelState and DiffusionSampler"):
   blog, sampler bullet "commit").
 * IDLE    -- untouched.
 
-Readings where the pages are silent or disagree are listed in the design doc's
-readings table; the ones that change results are restated next to the code.
+Where the pages are silent or disagree, the reading taken is stated next to
+the code that depends on it.
 """
 
 from __future__ import annotations
@@ -347,6 +347,33 @@ def commit_rows(p: Params, st_in: State, row_mask):
         if row_mask[r]:
             commit_row(p, st, r)
     return st
+
+
+def anneal_temperature(step, temperature, t_max, t_min, n_steps, row_mask=None):
+    """Linear temperature anneal over the denoising steps of a block.
+
+    "DiffusionGemma Explained" (ML@Berkeley), section "Sampling", the
+    ``denoise`` listing: the temperature starts at t_max and moves by
+    (t_min - t_max) / max_denoising_steps after every step, so step k of the
+    block divides the logits by t_max + k (t_min - t_max) / N.
+    "DiffusionGemma-Lite DIFFUSION.html", section 4.2 item 4: tau(k) is
+    annealed linearly from temp_start to temp_end across the schedule.
+
+    Readings: k is the row's block-local step counter (0 at the first denoise
+    step of a block), clamped to [0, N] so that steps past the schedule keep
+    t_min; the value is the closed form in fp64, rounded once to fp32 (the
+    listing's repeated addition differs only below fp32 resolution).  Rows
+    with row_mask[r] == 0 keep their temperature.  Returns a new fp32 array.
+    """
+    out = np.asarray(temperature, dtype=np.float32).copy()
+    t_max = float(np.float32(t_max))
+    t_min = float(np.float32(t_min))
+    for r in range(out.shape[0]):
+        if row_mask is not None and not row_mask[r]:
+            continue
+        k = min(max(int(step[r]), 0), int(n_steps))
+        out[r] = np.float32(t_max + k * (t_min - t_max) / n_steps)
+    return out
 
 
 def new_state(p: Params, phase, request_id, temperature, rng_step=None):

@@ -416,3 +416,36 @@ def test_selfcond_non_feeding_rows_are_zero():
     logits = g.normal(0, 2, (B, C, V))
     out = selfcond.selfcond(logits, np.ones(B), E, np.array([True, False, True]))
     assert np.all(out[C:2 * C] == 0) and np.any(out[:C] != 0)
+
+
+# ---- temperature anneal ("DiffusionGemma Explained", "Sampling", the denoise
+# listing; "DiffusionGemma-Lite DIFFUSION.html", section 4.2 item 4)
+
+def test_anneal_endpoints_and_clamping():
+    from oracle import sampler as osam
+    steps = np.array([0, 24, 40, -3], dtype=np.int32)
+    T = osam.anneal_temperature(steps, np.zeros(4, np.float32), 0.8, 0.4, 24)
+    assert T[0] == np.float32(0.8) and T[3] == np.float32(0.8)
+    assert T[1] == np.float32(0.4) and T[2] == np.float32(0.4)
+
+
+def test_anneal_matches_the_listing_by_repeated_addition():
+    # the listing's loop: t = t_max, then t += (t_min - t_max) / N after each step
+    from oracle import sampler as osam
+    for t_max, t_min, N in [(0.8, 0.4, 24), (1.2, 0.6, 32), (0.5, 1.5, 7)]:
+        t = float(np.float32(t_max))
+        dt = (float(np.float32(t_min)) - t) / N
+        steps = np.arange(N + 1, dtype=np.int32)
+        T = osam.anneal_temperature(steps, np.zeros(N + 1, np.float32), t_max, t_min, N)
+        for k in range(N + 1):
+            assert abs(float(T[k]) - t) <= float(np.spacing(np.float32(t))), (t_max, t_min, N, k)
+            t += dt
+        d = np.diff(T.astype(np.float64))
+        assert np.all(d <= 0) if t_max > t_min else np.all(d >= 0)
+
+
+def test_anneal_leaves_masked_rows():
+    from oracle import sampler as osam
+    T0 = np.array([0.7, 0.9, 1.1], np.float32)
+    T = osam.anneal_temperature(np.array([5, 5, 5]), T0, 1.0, 0.5, 10, row_mask=[1, 0, 1])
+    assert T[1] == T0[1] and T[0] == np.float32(0.75) and T[2] == np.float32(0.75)
