@@ -446,6 +446,9 @@ def run_graph_loop(args, dev):
     def block(s_):
         dg.dg_init_canvas(p, st, mask, stream=s_)
         for k in range(steps + 1):
+            if args.anneal:
+                # linear anneal t_max -> t_min over the block's steps, on the device
+                dg.dg_anneal_temperature(p, st, 1.2, 0.6, steps, stream=s_)
             dg.dg_denoise_step(p, bufs[k], st, ws, stream=s_)
             dg.dg_selfcond_embed(p, bufs[k], st, E, out, ws, stream=s_)
 
@@ -474,12 +477,23 @@ def run_graph_loop(args, dev):
     torch.cuda.synchronize(dev)
     graph_ms = e0.elapsed_time(e1) / reps
     calls = steps + 1
+    anneal_us = None
+    if args.anneal:
+        n = 200
+        e0.record(stream)
+        for _ in range(n):
+            dg.dg_anneal_temperature(p, st, 1.2, 0.6, steps, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        anneal_us = e0.elapsed_time(e1) / n * 1e3
     return {"metric": "denoise-step latency, 1 canvas loop (24 steps + commit)",
             "value": graph_ms / calls * 1e3, "unit": "us/step (graph replay)",
             "higher_is_better": False, "eager_us_per_step": eager_ms / calls * 1e3,
             "graph_ms_per_block": graph_ms, "eager_ms_per_block": eager_ms, "blocks": reps,
             "config": {"workload": "1x256-V262144-bf16-d2816 loop", "steps": steps,
-                       "cap": steps, "temperature": T},
+                       "cap": steps, "temperature": T if not args.anneal else
+                       {"anneal": "linear", "t_max": 1.2, "t_min": 0.6, "n_steps": steps}},
+            "anneal_us_per_call": anneal_us,
             "device_status": int(st.device_status.item())}
 
 
@@ -550,6 +564,8 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the canvas count (sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (sweeps)")
+    ap.add_argument("--anneal", action="store_true",
+                    help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop"],
                     help="step: the throughput line (default); graph-loop: one-canvas loop latency")
     ap.add_argument("--cpu-oracle-leg", action="store_true", help=argparse.SUPPRESS)

@@ -92,6 +92,8 @@ def lib():
         L.dg_denoise_step_noalloc.restype = ctypes.c_int
         L.dg_debug_wait_record.argtypes = [vp]
         L.dg_debug_wait_record.restype = ctypes.c_int
+        L.dg_anneal_temperature.argtypes = [P, vp, vp, ctypes.c_float, ctypes.c_float, i32, vp, vp]
+        L.dg_anneal_temperature.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -241,6 +243,19 @@ def dg_commit(params: Params, state: State, row_mask: torch.Tensor, stream=None)
         raise ValueError("row_mask: want uint8 [batch]")
     _check(lib().dg_commit(ctypes.byref(params.c()), ctypes.byref(state.c()),
                            _ptr(row_mask), _stream_ptr(stream)), "dg_commit")
+
+
+def dg_anneal_temperature(params: Params, state: State, t_max: float, t_min: float,
+                          n_steps: int, row_mask: torch.Tensor | None = None, stream=None):
+    """Write state.temperature[r] = t_max + k (t_min - t_max) / n_steps from the
+    rows' block-local step counters k (clamped to [0, n_steps]); call it before
+    dg_denoise_step."""
+    if row_mask is not None and (row_mask.dtype != torch.uint8 or row_mask.numel() != params.batch):
+        raise ValueError("row_mask: want uint8 [batch]")
+    _check(lib().dg_anneal_temperature(ctypes.byref(params.c()), _ptr(state.step),
+                                       _ptr(state.temperature), float(t_max), float(t_min),
+                                       int(n_steps), _ptr(row_mask) if row_mask is not None else None,
+                                       _stream_ptr(stream)), "dg_anneal_temperature")
 
 
 def dg_denoise_step(params: Params, logits: torch.Tensor, state: State,

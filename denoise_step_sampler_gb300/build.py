@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libdg.so")
 
-SOURCES = ["dg_api.cu", "dg_vocab.cu", "dg_canvas.cu", "dg_selfcond.cu", "dg_noalloc.cu"]
+SOURCES = ["dg_api.cu", "dg_vocab.cu", "dg_canvas.cu", "dg_selfcond.cu", "dg_noalloc.cu",
+           "dg_anneal.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

@@ -107,6 +107,22 @@ int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
   return DG_OK;
 }
 
+int dg_anneal_temperature(const dg_params *p, const int32_t *step, float *temperature,
+                          float t_max, float t_min, int32_t n_steps, const uint8_t *row_mask,
+                          cudaStream_t stream) {
+  if (!params_ok(p) || !step || !temperature || n_steps < 1) return DG_ERR_INVALID_ARG;
+  if (!(t_max > 0.f) || !(t_min > 0.f) || !std::isfinite(t_max) || !std::isfinite(t_min))
+    return DG_ERR_INVALID_ARG;
+  if (!aligned(step, 4) || !aligned(temperature, 4)) return DG_ERR_INVALID_ARG;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  cudaGetLastError();
+  if (launch_anneal(p->batch, step, temperature, t_max, t_min, n_steps, row_mask, stream) !=
+      cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
 int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st, void *ws,
                     size_t ws_bytes, cudaStream_t stream) {
   if (!params_ok(p) || !state_ok_full(st) || !logits) return DG_ERR_INVALID_ARG;

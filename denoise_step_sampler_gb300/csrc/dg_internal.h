@@ -42,4 +42,9 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
 // (synchronous; diagnostics only).
 cudaError_t dg_selfcond_wait_record(uint32_t out[4]);
 
+// Temperature anneal over the rows of the batch (see dg_anneal_temperature).
+cudaError_t launch_anneal(int32_t B, const int32_t *step, float *temperature, float t_max,
+                          float t_min, int32_t n_steps, const uint8_t *row_mask,
+                          cudaStream_t s);
+
 }  // namespace dg

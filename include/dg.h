@@ -161,6 +161,24 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
 int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
               cudaStream_t stream);
 
+/* Linear temperature anneal over the denoising steps of a block:
+ *   temperature[r] = t_max + k (t_min - t_max) / n_steps,
+ * k = step[r] (the row's block-local step counter, dg_state.step) clamped to
+ * [0, n_steps], evaluated in fp64 and rounded once to fp32.
+ * Sources: "DiffusionGemma Explained" (ML@Berkeley), section "Sampling" (the
+ * denoise loop starts at t_max and moves by (t_min - t_max) / N per step);
+ * "DiffusionGemma-Lite DIFFUSION.html", section 4.2 item 4.
+ * Call it before dg_denoise_step so that the vocabulary pass, the canvas step
+ * and the self-conditioning feed of that step all read the same temperature.
+ * `step`: device [B] int32 (in), `temperature`: device [B] fp32 (out), both
+ * owned by the caller; `row_mask`: device [B] (nonzero = update the row) or
+ * NULL for every row.  t_max, t_min > 0 and finite, n_steps >= 1, else
+ * DG_ERR_INVALID_ARG with nothing enqueued.  One kernel launch; no
+ * counterpart to the state layout: the pages anneal on the host. */
+int dg_anneal_temperature(const dg_params *p, const int32_t *step, float *temperature,
+                          float t_max, float t_min, int32_t n_steps,
+                          const uint8_t *row_mask, cudaStream_t stream);
+
 /* dg_denoise_step without a workspace, for callers that cannot allocate
  * device memory (an engine whose device memory is all pre-planned by its own
  * pool, or a host application whose allocations belong to another

@@ -120,3 +120,23 @@ def test_binding_checks_shapes_before_calling():
     p = _params()
     with pytest.raises(ValueError):
         dg.dg_denoise_step(p, torch.zeros(10), dg.State.__new__(dg.State), torch.zeros(1))
+
+
+def test_anneal_arguments_are_rejected_on_host(L):
+    p = _params().c()
+    step = ctypes.c_void_p(0x7100)
+    temp = ctypes.c_void_p(0x7200)
+    ok = (ctypes.byref(p), step, temp, 0.8, 0.4, 24, None, None)
+    bad = [
+        (None,) + ok[1:],
+        ok[:1] + (None,) + ok[2:],
+        ok[:2] + (None,) + ok[3:],
+        ok[:3] + (0.0,) + ok[4:],
+        ok[:3] + (float("nan"),) + ok[4:],
+        ok[:4] + (-0.4,) + ok[5:],
+        ok[:4] + (float("inf"),) + ok[5:],
+        ok[:5] + (0,) + ok[6:],
+        ok[:1] + (ctypes.c_void_p(0x7101),) + ok[2:],   # misaligned int32 array
+    ]
+    for args in bad:
+        assert L.dg_anneal_temperature(*args) == dg.DG_ERR_INVALID_ARG, args
