@@ -43,6 +43,13 @@ PHASE_IDLE = 3
 
 NEAR_TIE = 1e-4  # gap below which an index decision is flagged, not compared
 
+# convergence rules
+STOP_ARGMAX_STABLE = 0   # argmax canvas unchanged for k steps and mean entropy below thr
+STOP_ENTROPY = 1         # mean entropy below thr for k consecutive steps
+# acceptance rules
+ACCEPT_ENTROPY_BUDGET = 0  # lowest-entropy positions within the entropy budget
+ACCEPT_MONOTONE = 1        # unchanged-or-stronger commits, frozen once committed
+
 
 @dataclass
 class Params:
@@ -54,6 +61,8 @@ class Params:
     conf_threshold: float
     stable_k: int
     step_cap: int
+    stop_rule: int = STOP_ARGMAX_STABLE
+    accept_rule: int = ACCEPT_ENTROPY_BUDGET
 
 
 @dataclass
@@ -80,6 +89,8 @@ class State:
     num_sampled: np.ndarray = None   # int32 [B]
     num_rejected: np.ndarray = None  # int32 [B]
     emitted: np.ndarray = None       # int32 [B, C]
+    committed: np.ndarray = None     # uint8 [B, C] (monotone rule)
+    prev_conf: np.ndarray = None     # float64 [B, C] (monotone rule)
 
     def copy(self):
         out = State(**{k: (None if v is None else np.array(v, copy=True))
@@ -96,6 +107,7 @@ class Flags:
     accept: np.ndarray = None    # bool [B]: acceptance cut within 1e-4
     converged: np.ndarray = None  # bool [B]: |mean H - thr| < 1e-4
     gaps: np.ndarray = None      # float64 [B, C]
+    commit: np.ndarray = None    # bool [B, C]: |conf - prev_conf| < 1e-4 (monotone rule)
 
 
 # --------------------------------------------------------------------------
@@ -220,6 +232,17 @@ def _ensure_outputs(st: State, B, C):
     if st.num_sampled is None: st.num_sampled = z((B,), np.int32)
     if st.num_rejected is None: st.num_rejected = z((B,), np.int32)
     if st.emitted is None: st.emitted = z((B, C), np.int32)
+    if st.committed is None: st.committed = z((B, C), np.uint8)
+    if st.prev_conf is None: st.prev_conf = z((B, C), np.float64, np.inf)
+
+
+def _reset_commit_state(p: Params, st: State, r: int):
+    """Start of a block under the monotone rule: nothing frozen, and no
+    previous confidence (reading: +inf, so that the first step commits
+    nothing -- it has no previous mode to compare with either)."""
+    if p.accept_rule == ACCEPT_MONOTONE:
+        st.committed[r] = 0
+        st.prev_conf[r] = np.inf
 
 
 def prefill_row(p: Params, st: State, r: int):
@@ -237,14 +260,23 @@ def prefill_row(p: Params, st: State, r: int):
     st.converged[r] = 0
     st.phase[r] = PHASE_DENOISE
     st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+    _reset_commit_state(p, st, r)
 
 
 def commit_row(p: Params, st: State, r: int):
     """Emit the clean argmax canvas of the last denoise step (vLLM blog: the
     committed tokens are the clean argmax prediction), then start the next
-    block from a fresh random canvas with reset counters."""
+    block from a fresh random canvas with reset counters.
+
+    Under the monotone rule the block's result is the frozen tokens where a
+    position committed and the last step's draw elsewhere
+    ("DiffusionGemma-Lite DIFFUSION.html", section 4.2 item 5: every position
+    ends with its best posterior guess even if it never committed)."""
     C, V = p.canvas_len, p.vocab
-    st.emitted[r] = st.argmax_prev[r]
+    if p.accept_rule == ACCEPT_MONOTONE:
+        st.emitted[r] = np.where(st.committed[r] != 0, st.canvas[r], st.cand[r])
+    else:
+        st.emitted[r] = st.argmax_prev[r]
     st.num_sampled[r] = C
     st.num_rejected[r] = 0
     st.canvas[r] = init_tokens(p.seed, st.request_id[r], st.rng_step[r], C, V)
@@ -254,6 +286,7 @@ def commit_row(p: Params, st: State, r: int):
     st.converged[r] = 0
     st.phase[r] = PHASE_DENOISE
     st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+    _reset_commit_state(p, st, r)
 
 
 def _vocab_job(args):
@@ -280,19 +313,30 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=m
         flags.gaps[r, i] = res.gap
         flags.cand[r, i] = res.gap < NEAR_TIE
         H[i] = res.entropy
-    acc, aflag = accept_mask(H, p.entropy_budget)
-    flags.accept[r] = aflag
-    st.accept[r] = acc.astype(np.uint8)
     R = renoise_tokens(p.seed, st.request_id[r], st.rng_step[r], C, V)
-    st.canvas[r] = np.where(acc, st.cand[r], R)
+    if p.accept_rule == ACCEPT_MONOTONE:
+        monotone_commit(st, r, H, R, flags)
+    else:
+        acc, aflag = accept_mask(H, p.entropy_budget)
+        flags.accept[r] = aflag
+        st.accept[r] = acc.astype(np.uint8)
+        st.canvas[r] = np.where(acc, st.cand[r], R)
     # convergence (vLLM blog; Technical Report "Adaptive stopping heuristic")
     same = bool(st.step[r] > 0 and np.all(st.argmax[r] == st.argmax_prev[r]))
-    st.stable[r] = st.stable[r] + 1 if same else 0
     Hbar = float(np.sum(H) / C)
+    if p.stop_rule == STOP_ENTROPY:
+        # "DiffusionGemma-Lite DIFFUSION.html", section 4.4: stop once the mean
+        # entropy has stayed below the threshold for stability_steps steps
+        st.stable[r] = st.stable[r] + 1 if Hbar < p.conf_threshold else 0
+    else:
+        st.stable[r] = st.stable[r] + 1 if same else 0
     st.mean_entropy[r] = Hbar
     st.step[r] = st.step[r] + 1
     st.argmax_prev[r] = st.argmax[r]
-    conv = (st.stable[r] >= p.stable_k and Hbar < p.conf_threshold) or st.step[r] >= p.step_cap
+    if p.stop_rule == STOP_ENTROPY:
+        conv = st.stable[r] >= p.stable_k or st.step[r] >= p.step_cap
+    else:
+        conv = (st.stable[r] >= p.stable_k and Hbar < p.conf_threshold) or st.step[r] >= p.step_cap
     flags.converged[r] = (not math.isnan(Hbar)) and abs(Hbar - p.conf_threshold) < NEAR_TIE
     st.converged[r] = 1 if conv else 0
     st.sc_valid[r] = 0 if conv else 1
@@ -300,6 +344,35 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=m
     st.num_sampled[r] = 0
     st.num_rejected[r] = C
     st.rng_step[r] = st.rng_step[r] + np.uint64(1)
+
+
+def monotone_commit(st: State, r: int, H, R, flags: Flags):
+    """The unchanged-or-stronger commit rule ("DiffusionGemma-Lite
+    DIFFUSION.html", section 4.2): a position commits when its posterior mode
+    equals the previous step's or its confidence (the largest probability,
+    1/s with s = sum exp(y - max y)) did not fall; a newly committed position
+    takes the step's draw, a position committed earlier keeps its token (never
+    overwritten), and every other position is re-noised to a uniform token.
+    Readings: on the first step of a block there is no previous mode (its
+    comparison is false) and the previous confidence is +inf, so nothing
+    commits; positions with an invalid distribution never commit and keep their
+    previous confidence.  ``accept`` marks the newly committed positions.
+    Called before argmax_prev is replaced by this step's argmax."""
+    valid = ~np.isnan(H)
+    conf = np.where(valid, 1.0 / np.where(valid, st.s[r], 1.0), np.nan)
+    first = st.step[r] == 0
+    unchanged = np.zeros_like(valid) if first else (st.argmax[r] == st.argmax_prev[r])
+    prev = st.prev_conf[r].astype(np.float64)
+    stronger = valid & (conf >= prev)
+    commit = valid & (unchanged | stronger)
+    was = st.committed[r] != 0
+    new = commit & ~was
+    st.canvas[r] = np.where(new, st.cand[r], np.where(was, st.canvas[r], R))
+    st.committed[r] = (was | new).astype(np.uint8)
+    st.prev_conf[r] = np.where(valid, conf, prev)
+    st.accept[r] = new.astype(np.uint8)
+    # the confidence comparison decides only where the mode changed
+    flags.commit[r] = valid & ~unchanged & ~was & (np.abs(conf - prev) < NEAR_TIE)
 
 
 def step(p: Params, st_in: State, logits, rows=None, mapper=map):
@@ -315,7 +388,8 @@ def step(p: Params, st_in: State, logits, rows=None, mapper=map):
     st = st_in.copy()
     _ensure_outputs(st, B, C)
     flags = Flags(cand=np.zeros((B, C), bool), accept=np.zeros(B, bool),
-                  converged=np.zeros(B, bool), gaps=np.full((B, C), np.inf))
+                  converged=np.zeros(B, bool), gaps=np.full((B, C), np.inf),
+                  commit=np.zeros((B, C), bool))
     for r in range(B):
         ph = int(st.phase[r])
         if ph == PHASE_PREFILL:

@@ -449,3 +449,96 @@ def test_anneal_leaves_masked_rows():
     T0 = np.array([0.7, 0.9, 1.1], np.float32)
     T = osam.anneal_temperature(np.array([5, 5, 5]), T0, 1.0, 0.5, 10, row_mask=[1, 0, 1])
     assert T[1] == T0[1] and T[0] == np.float32(0.75) and T[2] == np.float32(0.75)
+
+
+# ---- rule variants ("DiffusionGemma-Lite DIFFUSION.html": section 4.2, the
+# unchanged-or-stronger commit rule; section 4.4, entropy-only adaptive stop)
+
+def _peaked(C, V, hot, height):
+    """[C, V] logits: zeros except `height` at token hot[i] of position i."""
+    z = np.zeros((C, V))
+    z[np.arange(C), hot] = height
+    return z
+
+
+def test_entropy_stop_converges_on_entropy_alone():
+    # the argmax moves every step, so the argmax-stable rule never converges
+    # before the cap, while the entropy rule stops after stable_k low-entropy
+    # steps: steps 0, 1 are flat (mean H = ln V > thr), 2, 3, 4 are sharp
+    from oracle import sampler as osam
+    C, V, k = 4, 16, 3
+    for rule, expect in [(osam.STOP_ENTROPY, 5), (osam.STOP_ARGMAX_STABLE, 8)]:
+        p = osam.Params(batch=1, canvas_len=C, vocab=V, seed=3, entropy_budget=100.0,
+                        conf_threshold=0.3, stable_k=k, step_cap=8, stop_rule=rule)
+        st = osam.new_state(p, [osam.PHASE_DENOISE], [1], [1.0])
+        for t in range(8):
+            z = np.zeros((C, V)) if t < 2 else _peaked(C, V, (np.arange(C) + t) % V, 40.0)
+            st, _ = osam.step(p, st, [z])
+            if st.converged[0]:
+                break
+        assert t + 1 == expect, (rule, t + 1)
+        if rule == osam.STOP_ENTROPY:
+            assert st.stable[0] == k
+
+
+def test_monotone_first_step_commits_nothing():
+    from oracle import sampler as osam
+    C, V = 6, 32
+    p = osam.Params(batch=1, canvas_len=C, vocab=V, seed=5, entropy_budget=0.0,
+                    conf_threshold=0.0, stable_k=3, step_cap=10, accept_rule=osam.ACCEPT_MONOTONE)
+    st = osam.new_state(p, [osam.PHASE_PREFILL], [2], [1.0])
+    st, _ = osam.step(p, st, [None])
+    assert np.all(st.committed[0] == 0) and np.all(np.isinf(st.prev_conf[0]))
+    st1, _ = osam.step(p, st, [_peaked(C, V, np.arange(C), 30.0)])
+    assert np.all(st1.committed[0] == 0) and np.all(st1.accept[0] == 0)
+    R = osam.renoise_tokens(p.seed, st.request_id[0], st.rng_step[0], C, V)
+    assert np.array_equal(st1.canvas[0], R)
+
+
+def test_monotone_unchanged_or_stronger_by_hand():
+    # position 0: same mode, confidence falls -> commits (unchanged)
+    # position 1: new mode, confidence rises  -> commits (stronger)
+    # position 2: new mode, confidence falls  -> stays open, re-noised
+    from oracle import sampler as osam
+    C, V = 3, 8
+    p = osam.Params(batch=1, canvas_len=C, vocab=V, seed=9, entropy_budget=0.0,
+                    conf_threshold=-1.0, stable_k=3, step_cap=10, accept_rule=osam.ACCEPT_MONOTONE)
+    st = osam.new_state(p, [osam.PHASE_DENOISE], [4], [1.0])
+    z0 = np.zeros((C, V)); z0[0, 1] = 5.0; z0[1, 2] = 1.0; z0[2, 3] = 5.0
+    st, _ = osam.step(p, st, [z0])              # first step: nothing commits
+    z1 = np.zeros((C, V)); z1[0, 1] = 2.0; z1[1, 5] = 6.0; z1[2, 6] = 1.0
+    st2, _ = osam.step(p, st, [z1])
+    # confidences by hand: max p = e^a / (e^a + V - 1)
+    conf = lambda a: math.exp(a) / (math.exp(a) + V - 1)
+    assert abs(st2.prev_conf[0, 1] - conf(6.0)) < 1e-12
+    assert st.prev_conf[0, 1] == conf(1.0) or abs(st.prev_conf[0, 1] - conf(1.0)) < 1e-12
+    assert list(st2.committed[0]) == [1, 1, 0]
+    assert list(st2.accept[0]) == [1, 1, 0]
+    assert st2.canvas[0, 0] == st2.cand[0, 0] and st2.canvas[0, 1] == st2.cand[0, 1]
+    R = osam.renoise_tokens(p.seed, st.request_id[0], st.rng_step[0], C, V)
+    assert st2.canvas[0, 2] == R[2]
+
+
+def test_monotone_frozen_tokens_never_change_and_emission():
+    from oracle import sampler as osam
+    rs = np.random.default_rng(1)
+    C, V = 16, 24
+    p = osam.Params(batch=1, canvas_len=C, vocab=V, seed=11, entropy_budget=0.0,
+                    conf_threshold=-1.0, stable_k=99, step_cap=6, accept_rule=osam.ACCEPT_MONOTONE)
+    st = osam.new_state(p, [osam.PHASE_DENOISE], [7], [0.9])
+    frozen = {}
+    for t in range(6):
+        z = rs.normal(0, 1.5, (C, V)); z[:, 3] += 0.3 * t   # confidence tends to rise
+        prev = st
+        st, _ = osam.step(p, st, [z])
+        assert np.all(st.committed[0] >= prev.committed[0])
+        for i, tok in frozen.items():
+            assert st.canvas[0, i] == tok
+        for i in np.flatnonzero((st.committed[0] == 1) & (prev.committed[0] == 0)):
+            assert st.canvas[0, i] == st.cand[0, i]
+            frozen[i] = st.canvas[0, i]
+    assert st.phase[0] == osam.PHASE_COMMIT and frozen
+    out, _ = osam.step(p, st, [None])
+    want = np.where(st.committed[0] == 1, st.canvas[0], st.cand[0])
+    assert np.array_equal(out.emitted[0], want)
+    assert np.all(out.committed[0] == 0) and np.all(np.isinf(out.prev_conf[0]))
