@@ -240,7 +240,10 @@ def run_ours(args, rank, world, dev):
     p = dg.Params(batch=B, canvas_len=C, vocab=V,
                   logits_dtype=dg.DG_BF16 if dt == "bf16" else dg.DG_F32,
                   seed=SEED, entropy_budget=budget, conf_threshold=0.3, stable_k=3,
-                  step_cap=1 << 30)
+                  step_cap=1 << 30,
+                  stop_rule={"argmax": dg.DG_STOP_ARGMAX_STABLE, "entropy": dg.DG_STOP_ENTROPY}[args.stop_rule],
+                  accept_rule={"budget": dg.DG_ACCEPT_ENTROPY_BUDGET,
+                               "monotone": dg.DG_ACCEPT_MONOTONE}[args.accept_rule])
     logits = syn.boosted_logits(B * C, V, seed=SEED + rank, dtype=tdt, device=dev,
                                 boost_hi=boost).reshape(-1)
     E = syn.embedding(V, d, seed=SEED, device=dev)
@@ -367,7 +370,8 @@ def run_ours(args, rank, world, dev):
                           "outside the timed events" if flush is not None else
                           "inputs larger than L2 (logits %.2f GB, E %.2f GB); no flush") % (
                        logit_bytes / 1e9, V * d * 2 / 1e9),
-                   "parallelism": f"replicas x{world} (independent requests per GPU)"},
+                   "parallelism": f"replicas x{world} (independent requests per GPU)",
+                   "accept_rule": args.accept_rule, "stop_rule": args.stop_rule},
         "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16,
@@ -564,6 +568,10 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="override the canvas count (sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg (sweeps)")
+    ap.add_argument("--accept-rule", default="budget", choices=["budget", "monotone"],
+                    help="entropy-budget acceptance or the unchanged-or-stronger commit rule")
+    ap.add_argument("--stop-rule", default="argmax", choices=["argmax", "entropy"],
+                    help="argmax-stable convergence or the entropy-only stop")
     ap.add_argument("--anneal", action="store_true",
                     help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop"],

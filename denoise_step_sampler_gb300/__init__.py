@@ -30,6 +30,8 @@ DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_WORKSPACE, DG_ERR_CUDA = 0
 DG_ERR_SCRATCH_LIMIT = 5
 DG_PHASE_PREFILL, DG_PHASE_DENOISE, DG_PHASE_COMMIT, DG_PHASE_IDLE = 0, 1, 2, 3
 DG_F32, DG_BF16 = 0, 1
+DG_STOP_ARGMAX_STABLE, DG_STOP_ENTROPY = 0, 1
+DG_ACCEPT_ENTROPY_BUDGET, DG_ACCEPT_MONOTONE = 0, 1
 DG_DEV_NONFINITE_LOGITS, DG_DEV_BAD_TEMPERATURE, DG_DEV_BAD_TOKEN = 1, 2, 4
 DG_DEV_WAIT_TIMEOUT, DG_DEV_BAD_PHASE = 8, 16
 
@@ -46,7 +48,8 @@ class _CParams(ctypes.Structure):
         ("logits_dtype", ctypes.c_int32), ("logits_ld", ctypes.c_int64),
         ("seed", ctypes.c_uint64), ("entropy_budget", ctypes.c_float),
         ("conf_threshold", ctypes.c_float), ("stable_k", ctypes.c_int32),
-        ("step_cap", ctypes.c_int32),
+        ("step_cap", ctypes.c_int32), ("stop_rule", ctypes.c_int32),
+        ("accept_rule", ctypes.c_int32),
     ]
 
 
@@ -54,6 +57,7 @@ _STATE_FIELDS = [
     "phase", "request_id", "temperature", "rng_step", "step", "stable", "canvas",
     "argmax_prev", "cand", "argmax", "accept", "m", "s", "entropy", "mean_entropy",
     "converged", "sc_valid", "num_sampled", "num_rejected", "emitted", "device_status",
+    "committed", "prev_conf",
 ]
 
 
@@ -112,12 +116,15 @@ class Params:
     conf_threshold: float = 0.3
     stable_k: int = 3
     step_cap: int = 32
+    stop_rule: int = DG_STOP_ARGMAX_STABLE
+    accept_rule: int = DG_ACCEPT_ENTROPY_BUDGET
 
     def c(self) -> _CParams:
         return _CParams(self.batch, self.canvas_len, self.vocab, self.logits_dtype,
                         self.vocab if self.logits_ld is None else self.logits_ld,
                         self.seed & 0xFFFFFFFFFFFFFFFF, self.entropy_budget,
-                        self.conf_threshold, self.stable_k, self.step_cap)
+                        self.conf_threshold, self.stable_k, self.step_cap, self.stop_rule,
+                        self.accept_rule)
 
 
 class State:
@@ -153,6 +160,8 @@ class State:
         self.num_rejected = z(B, torch.int32)
         self.emitted = z(B * C, torch.int32)
         self.device_status = z(1, torch.int32)
+        self.committed = z(B * C, torch.uint8)
+        self.prev_conf = torch.full((B * C,), float("inf"), dtype=torch.float32, device=dev)
 
     _EXPECT = {
         "phase": (torch.uint8, "B"), "request_id": (torch.int64, "B"),
@@ -165,6 +174,7 @@ class State:
         "converged": (torch.uint8, "B"), "sc_valid": (torch.uint8, "B"),
         "num_sampled": (torch.int32, "B"), "num_rejected": (torch.int32, "B"),
         "emitted": (torch.int32, "BC"), "device_status": (torch.int32, "1"),
+        "committed": (torch.uint8, "BC"), "prev_conf": (torch.float32, "BC"),
     }
 
     def c(self) -> _CState:

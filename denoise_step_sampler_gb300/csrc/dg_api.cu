@@ -21,6 +21,9 @@ bool params_ok(const dg_params *p) {
   if (!std::isfinite(p->entropy_budget) || p->entropy_budget < 0.f) return false;
   if (std::isnan(p->conf_threshold)) return false;
   if (p->stable_k < 1 || p->step_cap < 1) return false;
+  if (p->stop_rule != DG_STOP_ARGMAX_STABLE && p->stop_rule != DG_STOP_ENTROPY) return false;
+  if (p->accept_rule != DG_ACCEPT_ENTROPY_BUDGET && p->accept_rule != DG_ACCEPT_MONOTONE)
+    return false;
   // positions and partial records must be addressable
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
   if (n_pos > ((int64_t)1 << 40)) return false;
@@ -69,6 +72,11 @@ bool state_ok_full(const dg_state *st) {
          st->emitted;
 }
 
+// The monotone commit rule keeps per-position commit state.
+bool rule_state_ok(const dg_params *p, const dg_state *st) {
+  return p->accept_rule != DG_ACCEPT_MONOTONE || (st->committed && st->prev_conf);
+}
+
 }  // namespace
 
 extern "C" {
@@ -85,7 +93,8 @@ size_t dg_workspace_bytes(const dg_params *p, int32_t d) {
 
 int dg_init_canvas(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
                    cudaStream_t stream) {
-  if (!params_ok(p) || !state_ok_phase_machine(st) || !row_mask) return DG_ERR_INVALID_ARG;
+  if (!params_ok(p) || !state_ok_phase_machine(st) || !row_mask || !rule_state_ok(p, st))
+    return DG_ERR_INVALID_ARG;
   const int dv = device_ok();
   if (dv != DG_OK) return dv;
   cudaGetLastError();
@@ -97,7 +106,8 @@ int dg_init_canvas(const dg_params *p, const dg_state *st, const uint8_t *row_ma
 int dg_commit(const dg_params *p, const dg_state *st, const uint8_t *row_mask,
               cudaStream_t stream) {
   if (!params_ok(p) || !state_ok_phase_machine(st) || !row_mask || !st->argmax_prev ||
-      !st->emitted)
+      !st->emitted || !rule_state_ok(p, st) ||
+      (p->accept_rule == DG_ACCEPT_MONOTONE && !st->cand))
     return DG_ERR_INVALID_ARG;
   const int dv = device_ok();
   if (dv != DG_OK) return dv;
@@ -125,7 +135,8 @@ int dg_anneal_temperature(const dg_params *p, const int32_t *step, float *temper
 
 int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st, void *ws,
                     size_t ws_bytes, cudaStream_t stream) {
-  if (!params_ok(p) || !state_ok_full(st) || !logits) return DG_ERR_INVALID_ARG;
+  if (!params_ok(p) || !state_ok_full(st) || !logits || !rule_state_ok(p, st))
+    return DG_ERR_INVALID_ARG;
   const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
   if (!aligned(logits, esz)) return DG_ERR_INVALID_ARG;
   const size_t need = denoise_ws_bytes(p);

@@ -1,15 +1,20 @@
 // K2 -- one CTA per request slot: the per-canvas half of the sampler step.
 //
 // DENOISE rows: merge the vocabulary-pass partials of each position into
-// (m, s, H, argmax, cand); sort the canvas's (H, i) pairs ascending with a
-// bitonic network in shared memory; exclusive prefix sum of the sorted
-// entropies in fp64; accept while it stays within the budget (the first
-// always) -- "DiffusionGemma Explained", section "Sampling", step 3; re-noise
-// rejected positions to uniform tokens (Technical Report section 3.3); the
-// convergence test and phase update (vLLM blog, "Entropy-bounded denoising"
-// and "Putting it together").
+// (m, s, H, argmax, cand); then, under the entropy-budget rule, sort the
+// canvas's (H, i) pairs ascending with a bitonic network in shared memory,
+// take the exclusive prefix sum of the sorted entropies in fp64 and accept
+// while it stays within the budget (the first always) -- "DiffusionGemma
+// Explained", section "Sampling", step 3; re-noise rejected positions to
+// uniform tokens (Technical Report section 3.3).  Under the monotone rule
+// ("DiffusionGemma-Lite DIFFUSION.html", section 4.2) each position commits
+// on an unchanged argmax or a confidence 1/s no lower than the last step's,
+// committed tokens stay frozen, the rest are re-noised.  Then the convergence
+// test of the stop rule and the phase update (vLLM blog, "Entropy-bounded
+// denoising" and "Putting it together"; Lite section 4.4).
 // PREFILL rows: a fresh uniform canvas.  COMMIT rows: emit the clean argmax
-// canvas, then a fresh canvas and reset counters.  IDLE rows: untouched.
+// canvas (monotone rule: the committed tokens and the last candidates
+// elsewhere), then a fresh canvas and reset counters.  IDLE rows: untouched.
 #include "dg_device.cuh"
 #include "dg_internal.h"
 
@@ -38,6 +43,7 @@ struct CanvasArgs {
   uint64_t seed;
   float budget, thr;
   int32_t stable_k, step_cap;
+  int32_t stop_rule, accept_rule;
   dg_state st;
   const Partial *part;
   int32_t n_chunks;
@@ -52,7 +58,7 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   __shared__ uint8_t sacc[kMaxC];
   __shared__ double swarp[32];
   __shared__ double soff[32];
-  __shared__ float sH[kMaxC];
+  __shared__ float sH[kMaxC], sS[kMaxC];
   __shared__ int32_t sAm[kMaxC], sCand[kMaxC];
 
   const int r = blockIdx.x;
@@ -81,10 +87,12 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   const uint64_t rs = st.rng_step[r];
   const int64_t base = (int64_t)r * C;
 
+  const bool monotone = a.accept_rule == DG_ACCEPT_MONOTONE;
   if (do_init || do_commit) {
     for (int i = tid; i < C; i += nt) {
       if (do_commit) {
         int32_t tok = st.argmax_prev[base + i];
+        if (monotone) tok = st.committed[base + i] ? st.canvas[base + i] : st.cand[base + i];
         if (tok < 0 || tok >= V) {
           atomicOr(st.device_status, (uint32_t)DG_DEV_BAD_TOKEN);
           tok = 0;
@@ -94,6 +102,10 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)i);
       st.canvas[base + i] =
           (int32_t)below((uint32_t)(stream_key(pk, kTagInit) >> 32), (uint32_t)V);
+      if (monotone) {  // a block starts with nothing committed and no confidence
+        st.committed[base + i] = 0;
+        st.prev_conf[base + i] = INFINITY;
+      }
     }
     __syncthreads();
     if (tid == 0) {
@@ -195,6 +207,7 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
         atomicOr(st.device_status, (uint32_t)DG_DEV_NONFINITE_LOGITS);
       }
       sH[i] = ok ? Hf : NAN;
+      sS[i] = ok ? S : NAN;
       sAm[i] = ok ? pam : 0;
       sCand[i] = ok ? pcand : 0;
       st.m[base + i] = m_out;
@@ -210,65 +223,94 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   const int32_t am = (tid < C) ? sAm[tid] : 0;
   const int32_t cand = (tid < C) ? sCand[tid] : 0;
 
-  // sort (H, i) ascending; invalid positions and padding sort last as +inf
-  skey[tid] = valid ? H : INFINITY;
-  sidx[tid] = tid;
-  __syncthreads();
-  for (int k = 2; k <= nt; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const int o = tid ^ j;
-      if (o > tid) {
-        const float ka = skey[tid], kb = skey[o];
-        const int32_t ia = sidx[tid], ib = sidx[o];
-        const bool gt = (ka > kb) || (ka == kb && ia > ib);
-        const bool up = ((tid & k) == 0);
-        if (gt == up) {
-          skey[tid] = kb;
-          skey[o] = ka;
-          sidx[tid] = ib;
-          sidx[o] = ia;
-        }
-      }
-      __syncthreads();
-    }
-  }
-
-  // exclusive prefix sum of the sorted entropies (fp64), then the budget rule
-  const double x = (double)skey[tid];
-  const double incl = warp_incl_scan(x, lane);
-  double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-  if (lane == 0) excl = 0.0;
-  if (lane == 31) swarp[warp] = incl;
-  __syncthreads();
-  if (tid == 0) {
-    double run = 0.0;
-    for (int w = 0; w < nwarps; ++w) {
-      soff[w] = run;
-      run += swarp[w];
-    }
-  }
-  __syncthreads();
-  const double E = soff[warp] + excl;
-  const bool acc_k = isfinite(x) && (tid == 0 || E <= (double)a.budget);
-  sacc[sidx[tid]] = acc_k ? 1 : 0;
-  __syncthreads();
-
-  // re-noise, accept mask, convergence
+  const int32_t step0 = st.step[r];
   int same = 1;
   double hsum = 0.0;
-  if (tid < C) {
-    const bool acc = sacc[tid] != 0;
-    st.accept[base + tid] = acc ? 1 : 0;
-    int32_t tok = cand;
-    if (!acc) {
-      const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)tid);
-      tok = (int32_t)below((uint32_t)(stream_key(pk, kTagRenoise) >> 32), (uint32_t)V);
+  if (monotone) {
+    if (tid < C) {
+      const int32_t prev_am = st.argmax_prev[base + tid];
+      const bool was = st.committed[base + tid] != 0;
+      const float conf = valid ? 1.f / sS[tid] : NAN;
+      const float pc = st.prev_conf[base + tid];
+      const bool unchanged = step0 > 0 && prev_am == am;
+      const bool nw = valid && (unchanged || conf >= pc) && !was;
+      int32_t tok = cand;
+      if (!nw) {
+        if (was) {
+          tok = st.canvas[base + tid];
+        } else {
+          const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)tid);
+          tok = (int32_t)below((uint32_t)(stream_key(pk, kTagRenoise) >> 32), (uint32_t)V);
+        }
+      }
+      st.canvas[base + tid] = tok;
+      st.committed[base + tid] = (was || nw) ? 1 : 0;
+      if (valid) st.prev_conf[base + tid] = conf;
+      st.accept[base + tid] = nw ? 1 : 0;
+      same = (prev_am == am) ? 1 : 0;
+      st.argmax_prev[base + tid] = am;
+      hsum = valid ? (double)H : (double)NAN;
     }
-    st.canvas[base + tid] = tok;
-    same = (st.argmax_prev[base + tid] == am) ? 1 : 0;
-    st.argmax_prev[base + tid] = am;
-    hsum = valid ? (double)H : (double)NAN;
+  } else {
+    // sort (H, i) ascending; invalid positions and padding sort last as +inf
+    skey[tid] = valid ? H : INFINITY;
+    sidx[tid] = tid;
+    __syncthreads();
+    for (int k = 2; k <= nt; k <<= 1) {
+      for (int j = k >> 1; j > 0; j >>= 1) {
+        const int o = tid ^ j;
+        if (o > tid) {
+          const float ka = skey[tid], kb = skey[o];
+          const int32_t ia = sidx[tid], ib = sidx[o];
+          const bool gt = (ka > kb) || (ka == kb && ia > ib);
+          const bool up = ((tid & k) == 0);
+          if (gt == up) {
+            skey[tid] = kb;
+            skey[o] = ka;
+            sidx[tid] = ib;
+            sidx[o] = ia;
+          }
+        }
+        __syncthreads();
+      }
+    }
+
+    // exclusive prefix sum of the sorted entropies (fp64), then the budget rule
+    const double x = (double)skey[tid];
+    const double incl = warp_incl_scan(x, lane);
+    double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+    if (lane == 0) excl = 0.0;
+    if (lane == 31) swarp[warp] = incl;
+    __syncthreads();
+    if (tid == 0) {
+      double run = 0.0;
+      for (int w = 0; w < nwarps; ++w) {
+        soff[w] = run;
+        run += swarp[w];
+      }
+    }
+    __syncthreads();
+    const double E = soff[warp] + excl;
+    const bool acc_k = isfinite(x) && (tid == 0 || E <= (double)a.budget);
+    sacc[sidx[tid]] = acc_k ? 1 : 0;
+    __syncthreads();
+
+    // re-noise, accept mask
+    if (tid < C) {
+      const bool acc = sacc[tid] != 0;
+      st.accept[base + tid] = acc ? 1 : 0;
+      int32_t tok = cand;
+      if (!acc) {
+        const uint64_t pk = position_key(a.seed, rid, rs, (uint64_t)tid);
+        tok = (int32_t)below((uint32_t)(stream_key(pk, kTagRenoise) >> 32), (uint32_t)V);
+      }
+      st.canvas[base + tid] = tok;
+      same = (st.argmax_prev[base + tid] == am) ? 1 : 0;
+      st.argmax_prev[base + tid] = am;
+      hsum = valid ? (double)H : (double)NAN;
+    }
   }
+  // convergence
   const int all_same = __syncthreads_and(same);
   const double wsum = warp_sum(hsum);
   if (lane == 0) swarp[warp] = wsum;
@@ -277,11 +319,17 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
     double tot = 0.0;
     for (int w = 0; w < nwarps; ++w) tot += swarp[w];
     const double hbar = tot / (double)C;
-    const int32_t step0 = st.step[r];
-    const bool same_row = (step0 > 0) && all_same;
-    const int32_t stable = same_row ? st.stable[r] + 1 : 0;
     const int32_t step1 = step0 + 1;
-    const bool conv = (stable >= a.stable_k && hbar < (double)a.thr) || step1 >= a.step_cap;
+    int32_t stable;
+    bool conv;
+    if (a.stop_rule == DG_STOP_ENTROPY) {
+      stable = hbar < (double)a.thr ? st.stable[r] + 1 : 0;
+      conv = stable >= a.stable_k || step1 >= a.step_cap;
+    } else {
+      const bool same_row = (step0 > 0) && all_same;
+      stable = same_row ? st.stable[r] + 1 : 0;
+      conv = (stable >= a.stable_k && hbar < (double)a.thr) || step1 >= a.step_cap;
+    }
     st.stable[r] = stable;
     st.step[r] = step1;
     st.mean_entropy[r] = (float)hbar;
@@ -317,6 +365,8 @@ cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Par
   a.thr = p.conf_threshold;
   a.stable_k = p.stable_k;
   a.step_cap = p.step_cap;
+  a.stop_rule = p.stop_rule;
+  a.accept_rule = p.accept_rule;
   a.st = st;
   a.part = part;
   a.n_chunks = n_chunks;

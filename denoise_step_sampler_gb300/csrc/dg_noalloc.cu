@@ -56,21 +56,25 @@ bool params_ok(const dg_params *p) {
   if (!(p->entropy_budget >= 0.f) || p->entropy_budget > 3.0e38f) return false;
   if (p->conf_threshold != p->conf_threshold) return false;
   if (p->stable_k < 1 || p->step_cap < 1) return false;
+  if (p->stop_rule != DG_STOP_ARGMAX_STABLE && p->stop_rule != DG_STOP_ENTROPY) return false;
+  if (p->accept_rule != DG_ACCEPT_ENTROPY_BUDGET && p->accept_rule != DG_ACCEPT_MONOTONE)
+    return false;
   return true;
 }
 
-bool state_ok(const dg_state *st) {
+bool state_ok(const dg_params *p, const dg_state *st) {
   return st && st->phase && st->request_id && st->temperature && st->rng_step && st->step &&
          st->stable && st->canvas && st->argmax_prev && st->cand && st->argmax && st->accept &&
          st->m && st->s && st->entropy && st->mean_entropy && st->converged && st->sc_valid &&
-         st->num_sampled && st->num_rejected && st->emitted && st->device_status;
+         st->num_sampled && st->num_rejected && st->emitted && st->device_status &&
+         (p->accept_rule != DG_ACCEPT_MONOTONE || (st->committed && st->prev_conf));
 }
 
 }  // namespace
 
 extern "C" int dg_denoise_step_noalloc(const dg_params *p, const void *logits, const dg_state *st,
                                        cudaStream_t stream) {
-  if (!params_ok(p) || !state_ok(st) || !logits) return DG_ERR_INVALID_ARG;
+  if (!params_ok(p) || !state_ok(p, st) || !logits) return DG_ERR_INVALID_ARG;
   const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
   if (reinterpret_cast<uintptr_t>(logits) % esz != 0) return DG_ERR_INVALID_ARG;
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;

@@ -64,6 +64,29 @@ enum { DG_PHASE_PREFILL = 0, DG_PHASE_DENOISE = 1, DG_PHASE_COMMIT = 2, DG_PHASE
 /* Element types. */
 enum { DG_F32 = 0, DG_BF16 = 1 };
 
+/* Convergence rules (dg_params.stop_rule).
+ * DG_STOP_ARGMAX_STABLE: the argmax canvas unchanged for stable_k consecutive
+ *   steps and the mean entropy below conf_threshold ("DiffusionGemma
+ *   Explained", "Sampling"; vLLM blog, "Entropy-bounded denoising");
+ * DG_STOP_ENTROPY: the mean entropy below conf_threshold for stable_k
+ *   consecutive steps ("DiffusionGemma-Lite DIFFUSION.html", section 4.4).
+ * Either rule also stops at step_cap. */
+enum { DG_STOP_ARGMAX_STABLE = 0, DG_STOP_ENTROPY = 1 };
+
+/* Acceptance rules (dg_params.accept_rule).
+ * DG_ACCEPT_ENTROPY_BUDGET: positions by ascending (H, i) accepted while the
+ *   exclusive prefix sum of entropies is <= entropy_budget, the first always;
+ *   the rest re-noised ("DiffusionGemma Explained", "Sampling", step 3).
+ * DG_ACCEPT_MONOTONE: unchanged-or-stronger commits ("DiffusionGemma-Lite
+ *   DIFFUSION.html", section 4.2): a position commits when its argmax equals
+ *   the previous step's or its confidence (largest probability, 1/s) is >=
+ *   the previous step's; a newly committed position takes the Gumbel-max
+ *   candidate, an earlier committed one keeps its token, every other one is
+ *   re-noised.  A block starts with nothing committed and prev_conf = +inf
+ *   (so its first step commits nothing); commit rows emit the committed tokens
+ *   and the last candidates elsewhere.  Needs dg_state.committed / prev_conf. */
+enum { DG_ACCEPT_ENTROPY_BUDGET = 0, DG_ACCEPT_MONOTONE = 1 };
+
 /* Scalar parameters of a call (host memory, read during the call only). */
 typedef struct {
   int32_t batch;          /* B >= 1 request slots                                */
@@ -74,8 +97,10 @@ typedef struct {
   uint64_t seed;          /* random-number seed of the whole run                 */
   float entropy_budget;   /* nats, finite, >= 0 (acceptance budget)              */
   float conf_threshold;   /* nats; converge when mean entropy < this (not NaN)   */
-  int32_t stable_k;       /* >= 1 consecutive equal argmax canvases              */
+  int32_t stable_k;       /* >= 1 consecutive steps the stop rule asks for       */
   int32_t step_cap;       /* >= 1 maximum denoise steps per block                */
+  int32_t stop_rule;      /* DG_STOP_* (0 = argmax-stable)                       */
+  int32_t accept_rule;    /* DG_ACCEPT_* (0 = entropy budget)                    */
 } dg_params;
 
 /* Per-request state: device arrays, preallocated by the caller and updated in
@@ -88,12 +113,12 @@ typedef struct {
   const float *temperature;    /* [B]   in   T_r > 0 (caller anneals it if wanted)   */
   uint64_t *rng_step;          /* [B]   in/out +1 per processed call, never reset    */
   int32_t *step;               /* [B]   in/out denoise steps in the current block    */
-  int32_t *stable;             /* [B]   in/out consecutive equal argmax canvases     */
+  int32_t *stable;             /* [B]   in/out consecutive steps meeting the stop rule */
   int32_t *canvas;             /* [B*C] out  next tokens (accepted cand or re-noise) */
   int32_t *argmax_prev;        /* [B*C] in/out argmax canvas of the last step        */
   int32_t *cand;               /* [B*C] out  Gumbel-max candidates                   */
   int32_t *argmax;             /* [B*C] out  clean argmax of this step               */
-  uint8_t *accept;             /* [B*C] out  1 = accepted position                   */
+  uint8_t *accept;             /* [B*C] out  1 = accepted (newly committed) position */
   float *m;                    /* [B*C] out  max_v z_v / T   (NaN if invalid)        */
   float *s;                    /* [B*C] out  sum_v exp(z_v/T - m)                   */
   float *entropy;              /* [B*C] out  H in nats      (NaN if invalid)        */
@@ -104,6 +129,9 @@ typedef struct {
   int32_t *num_rejected;       /* [B]   out  C (denoise) or 0                        */
   int32_t *emitted;            /* [B*C] out  tokens emitted by commit rows           */
   uint32_t *device_status;     /* [1]   in/out sticky DG_DEV_* bits                  */
+  uint8_t *committed;          /* [B*C] in/out frozen positions (DG_ACCEPT_MONOTONE;
+                                  may be NULL under the other rule)                 */
+  float *prev_conf;            /* [B*C] in/out last step's confidence (same)        */
 } dg_state;
 
 /* Bytes of caller workspace needed by dg_denoise_step and, if d > 0, by

@@ -59,7 +59,8 @@ def oracle_params(p: dg.Params) -> osam.Params:
     return osam.Params(batch=p.batch, canvas_len=p.canvas_len, vocab=p.vocab, seed=p.seed,
                        entropy_budget=float(np.float32(p.entropy_budget)),
                        conf_threshold=float(np.float32(p.conf_threshold)),
-                       stable_k=p.stable_k, step_cap=p.step_cap)
+                       stable_k=p.stable_k, step_cap=p.step_cap, stop_rule=p.stop_rule,
+                       accept_rule=p.accept_rule)
 
 
 def oracle_state(snap: dict, p: dg.Params) -> osam.State:
@@ -72,6 +73,9 @@ def oracle_state(snap: dict, p: dg.Params) -> osam.State:
         canvas=snap["canvas"].reshape(B, C).copy(), argmax_prev=snap["argmax_prev"].reshape(B, C).copy())
     osam._ensure_outputs(st, B, C)
     st.emitted = snap["emitted"].reshape(B, C).copy()
+    st.cand = snap["cand"].reshape(B, C).copy()
+    st.committed = snap["committed"].reshape(B, C).copy()
+    st.prev_conf = snap["prev_conf"].reshape(B, C).astype(np.float64)
     return st
 
 
@@ -110,6 +114,8 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
                 assert g[k][r] == getattr(ost, k)[r], (r, k)
             if ph == dg.DG_PHASE_COMMIT:
                 assert np.array_equal(g["emitted"][sl], ost.emitted[r]), (r, "emitted")
+            if p.accept_rule == dg.DG_ACCEPT_MONOTONE:
+                assert np.all(g["committed"][sl] == 0) and np.all(np.isinf(g["prev_conf"][sl])), r
             continue
         # DENOISE
         valid = ~np.isnan(ost.entropy[r])
@@ -126,7 +132,17 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
         fc = flags.cand[r]
         n_flag["cand"] += int(fc.sum())
         assert np.array_equal(g["cand"][sl][~fc], ost.cand[r][~fc]), (r, "cand")
-        if flags.accept[r]:
+        if p.accept_rule == dg.DG_ACCEPT_MONOTONE:
+            fcm = flags.commit[r]
+            n_flag["accept"] += int(fcm.sum())
+            ok = ~fcm
+            assert np.array_equal(g["accept"][sl][ok], ost.accept[r][ok]), (r, "accept")
+            assert np.array_equal(g["committed"][sl][ok], ost.committed[r][ok]), (r, "committed")
+            ok &= ~(fc & (ost.accept[r] == 1))
+            assert np.array_equal(g["canvas"][sl][ok], ost.canvas[r][ok]), (r, "canvas")
+            rel = np.abs(g["prev_conf"][sl][v] / ost.prev_conf[r][v] - 1.0)
+            assert np.all(rel <= S_RTOL), (r, "prev_conf", float(rel.max()))
+        elif flags.accept[r]:
             n_flag["accept"] += 1
         else:
             assert np.array_equal(g["accept"][sl], ost.accept[r]), (r, "accept")
