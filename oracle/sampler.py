@@ -63,6 +63,8 @@ class Params:
     step_cap: int
     stop_rule: int = STOP_ARGMAX_STABLE
     accept_rule: int = ACCEPT_ENTROPY_BUDGET
+    softcap: float = 0.0       # c of the logit softcap; 0 = logits used as stored
+    embed_scale: float = 0.0   # factor on the self-conditioning feed; 0 = 1
 
 
 @dataclass
@@ -123,6 +125,18 @@ class PositionResult:
     argmax: int
     cand: int
     gap: float
+
+
+def softcap(z, c):
+    """Logit softcapping ("The Annotated DiffusionGemma", "Putting Them
+    together" / "Logit Softcapping"): z_capped = c tanh(z / c), applied to the
+    final logits before anything reads them.  float64; c = 0 leaves ``z``
+    unchanged.  tanh maps +-inf to +-1, so infinite logits become +-c; NaN
+    stays NaN."""
+    z = np.asarray(z, dtype=np.float64)
+    if c == 0:
+        return z
+    return c * np.tanh(z / c)
 
 
 def gumbel_keys(seed, request_id, rng_step, position):
@@ -290,10 +304,11 @@ def commit_row(p: Params, st: State, r: int):
 
 
 def _vocab_job(args):
-    """One position's vocabulary pass (a picklable unit for a process pool)."""
-    z, T, seed, rid, rstep, i = args
+    """One position's vocabulary pass (a picklable unit for a process pool).
+    The softcap, when set, is applied to the stored logits first."""
+    z, T, seed, rid, rstep, i, cap = args
     ka, kb, kc = gumbel_keys(seed, rid, rstep, i)
-    return vocab_pass(z, T, ka, kb, kc)
+    return vocab_pass(softcap(z, cap), T, ka, kb, kc)
 
 
 def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=map):
@@ -302,7 +317,8 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=m
     process pool's ``map``)."""
     C, V = p.canvas_len, p.vocab
     T = float(st.temperature[r])
-    jobs = [(logits_row[i], T, p.seed, st.request_id[r], st.rng_step[r], i) for i in range(C)]
+    jobs = [(logits_row[i], T, p.seed, st.request_id[r], st.rng_step[r], i, p.softcap)
+            for i in range(C)]
     H = np.empty(C)
     for i, res in enumerate(mapper(_vocab_job, jobs)):
         st.m[r, i] = res.m

@@ -3,9 +3,12 @@ package docstring).
 
 Technical Report section 3.2, eq. 6: p0 = Softmax(L_t / tau_t) and the next
 self-conditioning signal is FFW(p0 E), E the V x d token embedding.  This
-function computes the contraction p0 E only; the feed-forward network, the
-embedding scale and the add + RMSNorm around it are model side
-("DiffusionGemma Explained", "Self-conditioning").
+module computes the contraction p0 E, optionally times the embedding scale
+("The Annotated DiffusionGemma", the model's forward: the probabilities times
+W_embed, times embed_scale) and with p0 taken over softcapped logits ("Logit
+Softcapping" on the same page).  The feed-forward network and the add +
+RMSNorm around it are model side ("DiffusionGemma Explained",
+"Self-conditioning").
 
 Rows that do not feed a next denoise step get zeros: the first decode step
 sees all-zero self-conditioning ("DiffusionGemma Explained"), and the encoder
@@ -15,6 +18,8 @@ prefill / commit passes see it zeroed (vLLM blog, "Self-conditioning").
 from __future__ import annotations
 
 import numpy as np
+
+from oracle.sampler import softcap as _softcap
 
 
 def softmax_rows(z, T):
@@ -32,21 +37,23 @@ def softmax_rows(z, T):
     return out
 
 
-def selfcond_rows(z, T, E):
+def selfcond_rows(z, T, E, cap=0.0, scale=0.0):
     """p0 E for the rows of ``z`` ([n, V]) at temperature ``T`` with the
-    embedding ``E`` ([V, d], widened exactly to float64)."""
-    P = softmax_rows(z, T)
-    return P @ np.asarray(E, dtype=np.float64)
+    embedding ``E`` ([V, d], widened exactly to float64).  ``cap`` > 0
+    softcaps the logits first; ``scale`` multiplies the result (0 means 1)."""
+    P = softmax_rows(_softcap(z, cap), T)
+    out = P @ np.asarray(E, dtype=np.float64)
+    return out * scale if scale != 0 else out
 
 
-def selfcond(logits, temperature, E, feeds):
+def selfcond(logits, temperature, E, feeds, cap=0.0, scale=0.0):
     """Full [B*C, d] output.  ``logits`` [B, C, V]; ``temperature`` [B];
     ``feeds`` [B] bool: rows that ran a denoise step and did not converge.
-    Other rows are zero."""
+    Other rows are zero.  ``cap`` and ``scale`` as in ``selfcond_rows``."""
     B, C, _ = logits.shape
     d = E.shape[1]
     out = np.zeros((B * C, d))
     for r in range(B):
         if feeds[r]:
-            out[r * C:(r + 1) * C] = selfcond_rows(logits[r], float(temperature[r]), E)
+            out[r * C:(r + 1) * C] = selfcond_rows(logits[r], float(temperature[r]), E, cap, scale)
     return out

@@ -42,7 +42,7 @@ def _positions_match(p, snap, host_logits, T, rid, rstep, idx):
     """Per-position outputs of sampled positions (flat indices) vs the oracle."""
     C = p.canvas_len
     jobs = [(host_logits[q].astype(np.float64), float(T[q // C]), p.seed, rid[q // C],
-             rstep[q // C], q % C) for q in idx]
+             rstep[q // C], q % C, p.softcap) for q in idx]
     res = pmap(osam._vocab_job, jobs)
     n_flag = 0
     for q, r in zip(idx, res):

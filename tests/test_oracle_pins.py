@@ -542,3 +542,81 @@ def test_monotone_frozen_tokens_never_change_and_emission():
     want = np.where(st.committed[0] == 1, st.canvas[0], st.cand[0])
     assert np.array_equal(out.emitted[0], want)
     assert np.all(out.committed[0] == 0) and np.all(np.isinf(out.prev_conf[0]))
+
+
+# ---- logit softcap and embedding scale ("The Annotated DiffusionGemma",
+# "Logit Softcapping" and the model's forward)
+
+def _tanh_by_exp(x):
+    """tanh from its exponential definition, (e^2x - 1) / (e^2x + 1)."""
+    e = math.exp(2.0 * x)
+    return (e - 1.0) / (e + 1.0)
+
+
+@pytest.mark.parametrize("c", [30.0, 5.0, 0.75])
+def test_softcap_closed_forms(c):
+    # at z = +-c the cap is +-c tanh(1); at z = c/2 it is c tanh(1/2)
+    z = np.array([c, -c, 0.5 * c, 0.0])
+    got = sampler.softcap(z, c)
+    want = [c * _tanh_by_exp(1.0), -c * _tanh_by_exp(1.0), c * _tanh_by_exp(0.5), 0.0]
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
+    # small logits are essentially unchanged: z - z^3 / (3 c^2) to third order
+    small = np.array([1e-3, -2e-3, 5e-4]) * c
+    assert np.allclose(sampler.softcap(small, c), small - small ** 3 / (3 * c * c), rtol=1e-11)
+    # large logits approach +-c, infinite ones reach it; NaN stays NaN
+    big = sampler.softcap(np.array([1e6 * c, -1e6 * c, np.inf, -np.inf, np.nan]), c)
+    assert big[0] == c and big[1] == -c and big[2] == c and big[3] == -c and np.isnan(big[4])
+
+
+def test_softcap_is_odd_monotone_and_bounded():
+    g = np.random.default_rng(21)
+    c = 30.0
+    z = np.sort(g.normal(0, 40, 4001))
+    y = sampler.softcap(z, c)
+    assert np.all(np.diff(y) >= 0)
+    assert np.array_equal(sampler.softcap(-z, c), -y)
+    assert np.all(np.abs(y) <= np.minimum(np.abs(z), c))
+    assert np.array_equal(sampler.softcap(z, 0.0), z)  # c = 0: no cap
+
+
+def test_step_with_softcap_equals_step_on_capped_logits():
+    """The sampler reads the capped logits and nothing else: a capped step is
+    an uncapped step on c tanh(z / c) (built here from the exponential form)."""
+    g = np.random.default_rng(22)
+    C, V, c = 8, 40, 3.0
+    z = g.normal(0, 4, (2, C, V))
+    zc = np.vectorize(lambda x: c * _tanh_by_exp(x / c))(z)
+    base = dict(batch=2, canvas_len=C, vocab=V, seed=77, entropy_budget=12.0,
+                conf_threshold=0.3, stable_k=2, step_cap=8)
+    pc = sampler.Params(**base, softcap=c)
+    p0 = sampler.Params(**base)
+    st = sampler.new_state(pc, [sampler.PHASE_DENOISE] * 2, [4, 5], [0.9, 1.3])
+    a, _ = sampler.step(pc, st, z)
+    b, _ = sampler.step(p0, st, zc)
+    for k in ("canvas", "cand", "argmax", "accept", "stable", "phase"):
+        assert np.array_equal(getattr(a, k), getattr(b, k)), k
+    for k in ("m", "s", "entropy", "mean_entropy"):
+        assert np.allclose(getattr(a, k), getattr(b, k), rtol=1e-13, atol=1e-13), k
+    # the cap changes the result: c = 3 squeezes these logits hard
+    u, _ = sampler.step(p0, st, z)
+    assert not np.allclose(u.entropy, a.entropy)
+
+
+def test_selfcond_softcap_and_scale_by_hand():
+    # V = 3, one row: p = exp(cap(z)) / sum, done term by term
+    c, T, scale = 2.0, 0.5, math.sqrt(7.0)
+    z = np.array([[1.0, -3.0, 0.25]])
+    E = np.array([[1.0, 0.0], [0.0, 2.0], [-1.0, 1.0]])
+    w = [math.exp(c * _tanh_by_exp(x / c) / T) for x in z[0]]
+    s = sum(w)
+    want = [scale * (w[0] * 1.0 + w[2] * -1.0) / s, scale * (w[1] * 2.0 + w[2] * 1.0) / s]
+    got = selfcond.selfcond_rows(z, T, E, cap=c, scale=scale)
+    assert np.allclose(got[0], want, rtol=1e-14)
+    # scale 0 means 1; the scale is linear
+    g = np.random.default_rng(23)
+    L, E2 = g.normal(0, 3, (2, 4, 30)), g.normal(0, 0.02, (30, 6))
+    one = selfcond.selfcond(L, np.ones(2), E2, np.array([True, True]), cap=5.0)
+    assert np.array_equal(one, selfcond.selfcond(L, np.ones(2), E2, np.array([True, True]),
+                                                 cap=5.0, scale=1.0))
+    assert np.allclose(selfcond.selfcond(L, np.ones(2), E2, np.array([True, True]), cap=5.0,
+                                         scale=3.5), 3.5 * one, rtol=1e-15, atol=0)
