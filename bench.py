@@ -143,10 +143,12 @@ def gpu_id_for(dev) -> str:
 
 # ---------------------------------------------------------- CPU oracle leg
 
-def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None = None):
+def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None = None,
+                      cap: float = 0.0, scale: float = 0.0):
     """Time the fp64 oracle on a bounded sample of the workload: P positions of
     canvas 0 (vocabulary pass each, canvas-level acceptance on their
-    entropies) plus their self-conditioning rows through one fp64 matmul.
+    entropies) plus their self-conditioning rows through one fp64 matmul,
+    with the logit softcap ``cap`` and embedding scale ``scale`` when set.
     Returns (positions/s, P, seconds)."""
     import torch
     from denoise_step_sampler_gb300 import synthetic as syn
@@ -166,9 +168,10 @@ def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None =
         H = []
         for i in range(zrows.shape[0]):
             ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
-            H.append(osam.vocab_pass(zrows[i].astype(np.float64), Tf, ka, kb, kc).entropy)
+            zc = osam.softcap(zrows[i].astype(np.float64), cap)
+            H.append(osam.vocab_pass(zc, Tf, ka, kb, kc).entropy)
         osam.accept_mask(np.resize(np.asarray(H), C), budget)
-        osc.selfcond_rows(zrows.astype(np.float64), Tf, E)
+        osc.selfcond_rows(zrows.astype(np.float64), Tf, E, cap=cap, scale=scale)
         return time.perf_counter() - t0
 
     # t(P) = fixed + P * per_position (the fp64 E read is the fixed part): size
@@ -185,11 +188,12 @@ def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None =
     return P / t, P, t
 
 
-def cpu_baseline_subprocess(wl_name: str, budget_s: float = 12.0):
+def cpu_baseline_subprocess(wl_name: str, budget_s: float = 12.0, cap: float = 0.0,
+                            scale: float = 0.0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-oracle-leg", "--workload", wl_name,
-           "--cpu-budget", str(budget_s)]
+           "--cpu-budget", str(budget_s), "--softcap", str(cap), "--embed-scale", str(scale)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
@@ -243,7 +247,8 @@ def run_ours(args, rank, world, dev):
                   step_cap=1 << 30,
                   stop_rule={"argmax": dg.DG_STOP_ARGMAX_STABLE, "entropy": dg.DG_STOP_ENTROPY}[args.stop_rule],
                   accept_rule={"budget": dg.DG_ACCEPT_ENTROPY_BUDGET,
-                               "monotone": dg.DG_ACCEPT_MONOTONE}[args.accept_rule])
+                               "monotone": dg.DG_ACCEPT_MONOTONE}[args.accept_rule],
+                  softcap=args.softcap, embed_scale=args.embed_scale)
     logits = syn.boosted_logits(B * C, V, seed=SEED + rank, dtype=tdt, device=dev,
                                 boost_hi=boost).reshape(-1)
     E = syn.embedding(V, d, seed=SEED, device=dev)
@@ -371,7 +376,8 @@ def run_ours(args, rank, world, dev):
                           "inputs larger than L2 (logits %.2f GB, E %.2f GB); no flush") % (
                        logit_bytes / 1e9, V * d * 2 / 1e9),
                    "parallelism": f"replicas x{world} (independent requests per GPU)",
-                   "accept_rule": args.accept_rule, "stop_rule": args.stop_rule},
+                   "accept_rule": args.accept_rule, "stop_rule": args.stop_rule,
+                   "softcap": args.softcap, "embed_scale": args.embed_scale},
         "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16,
@@ -394,7 +400,8 @@ def run_ours(args, rank, world, dev):
     }
     if not args.no_cpu_baseline:
         try:
-            cb = cpu_baseline_subprocess(args.workload if not args.batch else DEFAULT)
+            cb = cpu_baseline_subprocess(args.workload if not args.batch else DEFAULT,
+                                         cap=args.softcap, scale=args.embed_scale)
             line["cpu_baseline"] = {"value": cb["value"], "unit": "positions/s", "cores": 1,
                                     "kind": "oracle", "sample": cb["sample"]}
         except Exception as e:  # pragma: no cover
@@ -576,6 +583,10 @@ def main():
                     help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop"],
                     help="step: the throughput line (default); graph-loop: one-canvas loop latency")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="logit softcap c (c tanh(z / c) before the pass); 0 = off")
+    ap.add_argument("--embed-scale", type=float, default=0.0,
+                    help="factor on the self-conditioning feed (e.g. sqrt(d)); 0 = 1")
     ap.add_argument("--cpu-oracle-leg", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
@@ -583,7 +594,8 @@ def main():
         ap.error("--warmup must be >= 3")
 
     if args.cpu_oracle_leg:
-        rate, P, t = cpu_oracle_sample(args.workload, args.cpu_budget)
+        rate, P, t = cpu_oracle_sample(args.workload, args.cpu_budget, cap=args.softcap,
+                                       scale=args.embed_scale)
         print(json.dumps({"value": rate, "positions": P, "seconds": t,
                           "sample": f"{P} positions of canvas 0 of the same workload: vocab pass "
                                     f"+ self-cond rows (fp64 numpy, 1 thread), {t:.1f} s"}))

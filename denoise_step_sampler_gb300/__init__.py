@@ -49,7 +49,8 @@ class _CParams(ctypes.Structure):
         ("seed", ctypes.c_uint64), ("entropy_budget", ctypes.c_float),
         ("conf_threshold", ctypes.c_float), ("stable_k", ctypes.c_int32),
         ("step_cap", ctypes.c_int32), ("stop_rule", ctypes.c_int32),
-        ("accept_rule", ctypes.c_int32),
+        ("accept_rule", ctypes.c_int32), ("softcap", ctypes.c_float),
+        ("embed_scale", ctypes.c_float),
     ]
 
 
@@ -118,13 +119,15 @@ class Params:
     step_cap: int = 32
     stop_rule: int = DG_STOP_ARGMAX_STABLE
     accept_rule: int = DG_ACCEPT_ENTROPY_BUDGET
+    softcap: float = 0.0      # logit softcap c (0 = off)
+    embed_scale: float = 0.0  # factor on the self-conditioning feed (0 = 1)
 
     def c(self) -> _CParams:
         return _CParams(self.batch, self.canvas_len, self.vocab, self.logits_dtype,
                         self.vocab if self.logits_ld is None else self.logits_ld,
                         self.seed & 0xFFFFFFFFFFFFFFFF, self.entropy_budget,
                         self.conf_threshold, self.stable_k, self.step_cap, self.stop_rule,
-                        self.accept_rule)
+                        self.accept_rule, self.softcap, self.embed_scale)
 
 
 class State:

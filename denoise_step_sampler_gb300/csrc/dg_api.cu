@@ -24,6 +24,8 @@ bool params_ok(const dg_params *p) {
   if (p->stop_rule != DG_STOP_ARGMAX_STABLE && p->stop_rule != DG_STOP_ENTROPY) return false;
   if (p->accept_rule != DG_ACCEPT_ENTROPY_BUDGET && p->accept_rule != DG_ACCEPT_MONOTONE)
     return false;
+  if (!std::isfinite(p->softcap) || p->softcap < 0.f) return false;
+  if (!std::isfinite(p->embed_scale) || p->embed_scale < 0.f) return false;
   // positions and partial records must be addressable
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
   if (n_pos > ((int64_t)1 << 40)) return false;

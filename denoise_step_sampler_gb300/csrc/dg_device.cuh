@@ -70,6 +70,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Logit softcap c tanh(z / c), from tanh x = 1 - 2 / (e^(2x) + 1):
+// c - 2c / (2^(z k) + 1) with k = 2 log2(e) / c.  +-inf map to +-c and NaN
+// stays NaN.  The absolute error is a few 1e-7 c (ex2.approx and the rounded
+// reciprocal near e = 1, where the slope is largest).
+__device__ __forceinline__ float softcap_f(float z, float k, float c) {
+  const float e = ex2_approx(__fmul_rn(z, k));
+  return fmaf(-2.0f * c, __frcp_rn(__fadd_rn(e, 1.0f)), c);
+}
+
 // Packed pairs of fp32 (Blackwell f32x2 arithmetic).
 __device__ __forceinline__ uint64_t pack2(float lo, float hi) {
   uint64_t r;

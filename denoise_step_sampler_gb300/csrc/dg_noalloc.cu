@@ -59,6 +59,8 @@ bool params_ok(const dg_params *p) {
   if (p->stop_rule != DG_STOP_ARGMAX_STABLE && p->stop_rule != DG_STOP_ENTROPY) return false;
   if (p->accept_rule != DG_ACCEPT_ENTROPY_BUDGET && p->accept_rule != DG_ACCEPT_MONOTONE)
     return false;
+  if (!(p->softcap >= 0.f) || p->softcap > 3.0e38f) return false;
+  if (!(p->embed_scale >= 0.f) || p->embed_scale > 3.0e38f) return false;
   return true;
 }
 

@@ -287,6 +287,8 @@ struct GemmArgs {
   int32_t out_dtype;
   float *partial;  // [splits][rows][d] when splits > 1
   uint32_t *status;
+  float cap_k, cap_c;  // logit softcap: 2 log2(e) / c and c (capped kernels only)
+  float scale;         // factor on the output (the embedding scale; 1 = none)
 };
 
 __device__ __forceinline__ bool row_feeds(const GemmArgs &a, int64_t q, float &c, float &l2) {
@@ -375,6 +377,32 @@ __device__ __forceinline__ uint4 p_from_f32(const uint32_t (&w)[8], float c, flo
                     pack_bf16x2(p[6], p[7]));
 }
 
+// p from softcapped logits ("The Annotated DiffusionGemma", "Logit
+// Softcapping"): the same rebuild on c tanh(z / c) for the first `valid` of 8
+// bf16 (w[0..3]) or fp32 (w[0..7]) logits.
+__device__ __forceinline__ uint4 p_from_bf16_cap(const uint32_t (&w)[4], float c, float l2,
+                                                 int valid, float cap_k, float cap_c) {
+  float p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float z = __uint_as_float((j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16));
+    p[j] = (j < valid) ? ex2_approx(fmaf(softcap_f(z, cap_k, cap_c), c, -l2)) : 0.f;
+  }
+  return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                    pack_bf16x2(p[6], p[7]));
+}
+__device__ __forceinline__ uint4 p_from_f32_cap(const uint32_t (&w)[8], float c, float l2,
+                                                int valid, float cap_k, float cap_c) {
+  float p[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    p[j] = (j < valid)
+               ? ex2_approx(fmaf(softcap_f(__uint_as_float(w[j]), cap_k, cap_c), c, -l2))
+               : 0.f;
+  return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
+                    pack_bf16x2(p[6], p[7]));
+}
+
 // Byte offset of 16-byte chunk `ch` (0..7) of row `r` in a 128-byte-swizzled
 // K-major tile (8-row atoms of 1024 bytes).
 __device__ __forceinline__ uint32_t a_off(int r, int ch) {
@@ -383,8 +411,9 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
 
 // CL CTAs form a cluster over CL consecutive row tiles of one column tile and
 // one vocabulary split: each loads 1/CL of every E tile and multicasts it to
-// all CL, so E leaves L2 once per cluster instead of once per CTA.
-template <int CL>
+// all CL, so E leaves L2 once per cluster instead of once per CTA.  CAP: the
+// producers softcap the logits before the rebuild.
+template <int CL, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
                          const __grid_constant__ CUtensorMap tmap_z,
@@ -560,19 +589,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) v[j] = *reinterpret_cast<const uint4 *>(tileA + off[j]);
           if ((int64_t)(kb0 + i + 1) * BK <= (int64_t)a.V) {  // warp-uniform: block inside V
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              *reinterpret_cast<uint4 *>(tileA + off[j]) =
-                  ((okm >> j) & 1u) ? p_from_bf16_full(v[j], cc2[j], nl2[j])
-                                    : make_uint4(0u, 0u, 0u, 0u);
+            for (int j = 0; j < 4; ++j) {
+              uint4 pv = make_uint4(0u, 0u, 0u, 0u);
+              if ((okm >> j) & 1u) {
+                if constexpr (CAP) {
+                  const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                  pv = p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), 8, a.cap_k, a.cap_c);
+                } else {
+                  pv = p_from_bf16_full(v[j], cc2[j], nl2[j]);
+                }
+              }
+              *reinterpret_cast<uint4 *>(tileA + off[j]) = pv;
+            }
           } else {
             const int64_t rem = (int64_t)a.V - ((int64_t)(kb0 + i) * BK + ch * 8);
             const int valid = rem >= 8 ? 8 : (rem <= 0 ? 0 : (int)rem);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-              *reinterpret_cast<uint4 *>(tileA + off[j]) =
-                  ((okm >> j) & 1u) ? p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+              uint4 pv = make_uint4(0u, 0u, 0u, 0u);
+              if ((okm >> j) & 1u)
+                pv = CAP ? p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k, a.cap_c)
+                         : p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+              *reinterpret_cast<uint4 *>(tileA + off[j]) = pv;
             }
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -610,9 +649,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((okm >> j) & 1u) {
               if (a.dtype == DG_BF16) {
                 const uint32_t w[4] = {x[j].w[0], x[j].w[1], x[j].w[2], x[j].w[3]};
-                pv[j] = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                pv[j] = CAP ? p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k,
+                                              a.cap_c)
+                            : p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               } else {
-                pv[j] = p_from_f32(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                pv[j] = CAP ? p_from_f32_cap(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k,
+                                             a.cap_c)
+                            : p_from_f32(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               }
             }
           }
@@ -657,6 +700,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      } else if (a.splits == 1) {  // split partials are scaled by the reduction
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= a.scale;
       }
       if (q < a.rows && a.splits > 1 && run) {
         // (rows that do not feed get zeros from the reduction)
@@ -713,6 +759,10 @@ __global__ void selfcond_reduce_kernel(GemmArgs a) {
         acc.z += v.z;
         acc.w += v.w;
       }
+      acc.x *= a.scale;
+      acc.y *= a.scale;
+      acc.z *= a.scale;
+      acc.w *= a.scale;
     }
     if (a.out_dtype == DG_F32) {
       *reinterpret_cast<float4 *>(reinterpret_cast<float *>(a.out) + q * a.d + col) = acc;
@@ -782,7 +832,7 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
 }
 
 namespace {
-template <int CL>
+template <int CL, bool CAP>
 cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
                         const CUtensorMap &map_ep, const GemmArgs &a, int64_t grid,
                         cudaStream_t s) {
@@ -791,7 +841,7 @@ cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
   if (e != cudaSuccess) return e;
   static bool attr_set[64] = {false};
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CL>,
+    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CL, CAP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
@@ -809,7 +859,7 @@ cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL>, map_e, map_z, map_ep, a);
+  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL, CAP>, map_e, map_z, map_ep, a);
 }
 
 }  // namespace
@@ -881,13 +931,19 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.out_dtype = out_dtype;
   a.partial = reinterpret_cast<float *>(ws);
   a.status = st.device_status;
+  const bool cap = p.softcap > 0.f;
+  a.cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
+  a.cap_c = cap ? p.softcap : 0.f;
+  a.scale = p.embed_scale > 0.f ? p.embed_scale : 1.0f;
 
   const int64_t grid = (int64_t)plan.m_groups * plan.cluster * plan.n_tiles * plan.splits;
   cudaError_t e;
   if (plan.cluster == 2)
-    e = launch_gemm<2>(map_e, map_z, map_ep, a, grid, s);
+    e = cap ? launch_gemm<2, true>(map_e, map_z, map_ep, a, grid, s)
+            : launch_gemm<2, false>(map_e, map_z, map_ep, a, grid, s);
   else
-    e = launch_gemm<1>(map_e, map_z, map_ep, a, grid, s);
+    e = cap ? launch_gemm<1, true>(map_e, map_z, map_ep, a, grid, s)
+            : launch_gemm<1, false>(map_e, map_z, map_ep, a, grid, s);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

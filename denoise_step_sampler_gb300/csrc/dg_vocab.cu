@@ -377,6 +377,35 @@ template <int DT>
 __device__ __forceinline__ void load_group_scalar(const void *row, int64_t v, int n, float *z) {
   for (int j = 0; j < n; ++j) z[j] = load_scalar<DT>(row, v + j);
 }
+// The n (<= 8) logits of the group starting at column v (a multiple of 8) as
+// fp32, softcapped when CAP ("The Annotated DiffusionGemma", "Logit
+// Softcapping": every later step reads the capped value).  Whole groups of a
+// 16-byte-aligned row take vector loads.
+template <int DT, bool CAP>
+__device__ __forceinline__ void load_group(const void *row, bool aligned, int64_t v, int n,
+                                           float *z, float cap_k, float cap_c) {
+  if (aligned && n == 8) {
+    if (DT == DG_BF16) {
+      float w[8];
+      unpack_bf16x8(ld_stream(reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const uint16_t *>(row) + v)),
+                    w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) z[j] = w[j];
+    } else {
+      const uint4 *p = reinterpret_cast<const uint4 *>(reinterpret_cast<const float *>(row) + v);
+      const uint4 a = ld_stream(p), b = ld_stream(p + 1);
+      z[0] = __uint_as_float(a.x); z[1] = __uint_as_float(a.y);
+      z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
+      z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
+      z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
+    }
+  } else {
+    load_group_scalar<DT>(row, v, n, z);
+  }
+  if (CAP)
+    for (int j = 0; j < n; ++j) z[j] = softcap_f(z[j], cap_k, cap_c);
+}
 
 // Merge the 32 lanes' records; every lane ends with the warp result, its sums
 // relative to fl(zmax c).  Each lane's sums come relative to its own
@@ -424,11 +453,14 @@ __device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32
   }
 }
 
-template <int DT>
+// CAP: logits pass through the softcap (cap_k = 2 log2(e) / c, cap_c = c)
+// before any other use; capped calls take the per-group path.
+template <int DT, bool CAP>
 // 4 CTAs of 8 warps per SM: the register budget is capped at 64 per thread
 __global__ void __launch_bounds__(kWarps * 32, 4)
     vocab_pass_kernel(const void *__restrict__ logits, int64_t ld, int32_t V, int32_t C,
                       int64_t n_pos, int32_t chunk, int32_t n_chunks, uint64_t seed,
+                      float cap_k, float cap_c,
                       const uint8_t *__restrict__ phase, const uint64_t *__restrict__ request_id,
                       const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
                       Partial *__restrict__ part, uint32_t *__restrict__ status) {
@@ -497,7 +529,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
   Q.q = &s_queue[threadIdx.x >> 5][0];
   Q.head = 0;
   Q.count = 0;
-  if (aligned && DT == DG_BF16) {
+  if (!CAP && aligned && DT == DG_BF16) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
     const int rounds = n_full / 128;
     // Per round each lane holds 4 groups (32 logits).  The round's maximum
@@ -613,7 +645,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       }
       coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
     }
-  } else if (aligned) {
+  } else if (!CAP && aligned) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + 2 * (size_t)g0;
     const int rounds = n_full / 64;
     for (int rd = 0; rd < rounds; ++rd) {
@@ -660,7 +692,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       uint32_t h = 0;
       bool pass = false;
       if (q < n_full) {
-        load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
+        load_group<DT, CAP>(row, aligned, v0 + (int64_t)q * kGroup, 8, z, cap_k, cap_c);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
       coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
@@ -678,13 +710,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
     lane_init(L);
     for (int q = lane; q < n_full; q += 32) {
       float z[8];
-      load_group_scalar<DT>(row, v0 + (int64_t)q * kGroup, 8, z);
+      load_group<DT, CAP>(row, aligned, v0 + (int64_t)q * kGroup, 8, z, cap_k, cap_c);
       group_careful(z, 8, g0 + (uint32_t)q, c, K, L, flags);
     }
   }
   if (tail_n > 0 && lane == (n_full & 31)) {
     float z[8];
-    load_group_scalar<DT>(row, v0 + (int64_t)n_full * kGroup, tail_n, z);
+    load_group<DT, CAP>(row, false, v0 + (int64_t)n_full * kGroup, tail_n, z, cap_k, cap_c);
     group_careful(z, tail_n, g0 + (uint32_t)n_full, c, K, L, flags);
   }
   sums(L, s, t);
@@ -716,15 +748,21 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const int64_t warps = n_pos * n_chunks;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const bool cap = p.softcap > 0.f;
+  const float cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
+  const float cap_c = cap ? p.softcap : 0.f;
+#define DG_VOCAB_LAUNCH(DT, CAP)                                                              \
+  vocab_pass_kernel<DT, CAP><<<(unsigned)blocks, kWarps * 32, 0, s>>>(                        \
+      logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c, \
+      st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status)
   if (p.logits_dtype == DG_BF16) {
-    vocab_pass_kernel<DG_BF16><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
-        logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, st.phase,
-        st.request_id, st.temperature, st.rng_step, part, st.device_status);
+    if (cap) DG_VOCAB_LAUNCH(DG_BF16, true);
+    else DG_VOCAB_LAUNCH(DG_BF16, false);
   } else {
-    vocab_pass_kernel<DG_F32><<<(unsigned)blocks, kWarps * 32, 0, s>>>(
-        logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, st.phase,
-        st.request_id, st.temperature, st.rng_step, part, st.device_status);
+    if (cap) DG_VOCAB_LAUNCH(DG_F32, true);
+    else DG_VOCAB_LAUNCH(DG_F32, false);
   }
+#undef DG_VOCAB_LAUNCH
   return cudaGetLastError();
 }
 

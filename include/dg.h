@@ -101,6 +101,16 @@ typedef struct {
   int32_t step_cap;       /* >= 1 maximum denoise steps per block                */
   int32_t stop_rule;      /* DG_STOP_* (0 = argmax-stable)                       */
   int32_t accept_rule;    /* DG_ACCEPT_* (0 = entropy budget)                    */
+  float softcap;          /* c of the logit softcap z <- c tanh(z / c), applied to
+                             every stored logit before any other use ("The
+                             Annotated DiffusionGemma", "Logit Softcapping"):
+                             m, s, H, the argmax, the candidate and the
+                             self-conditioning softmax all see capped logits.
+                             0 = off; finite, >= 0                              */
+  float embed_scale;      /* factor on dg_selfcond_embed's output (the model's
+                             embedding scale on the probability-weighted
+                             embedding, "The Annotated DiffusionGemma", the
+                             forward pass); 0 = 1; finite, >= 0                 */
 } dg_params;
 
 /* Per-request state: device arrays, preallocated by the caller and updated in
@@ -119,7 +129,8 @@ typedef struct {
   int32_t *cand;               /* [B*C] out  Gumbel-max candidates                   */
   int32_t *argmax;             /* [B*C] out  clean argmax of this step               */
   uint8_t *accept;             /* [B*C] out  1 = accepted (newly committed) position */
-  float *m;                    /* [B*C] out  max_v z_v / T   (NaN if invalid)        */
+  float *m;                    /* [B*C] out  max_v z_v / T   (NaN if invalid; z after
+                                  the softcap when dg_params.softcap > 0)           */
   float *s;                    /* [B*C] out  sum_v exp(z_v/T - m)                   */
   float *entropy;              /* [B*C] out  H in nats      (NaN if invalid)        */
   float *mean_entropy;         /* [B]   out  mean of H over the canvas              */

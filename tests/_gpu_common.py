@@ -60,7 +60,8 @@ def oracle_params(p: dg.Params) -> osam.Params:
                        entropy_budget=float(np.float32(p.entropy_budget)),
                        conf_threshold=float(np.float32(p.conf_threshold)),
                        stable_k=p.stable_k, step_cap=p.step_cap, stop_rule=p.stop_rule,
-                       accept_rule=p.accept_rule)
+                       accept_rule=p.accept_rule, softcap=float(np.float32(p.softcap)),
+                       embed_scale=float(np.float32(p.embed_scale)))
 
 
 def oracle_state(snap: dict, p: dg.Params) -> osam.State:

@@ -62,7 +62,9 @@ def test_workspace_query(L):
     for bad in (dict(batch=0), dict(canvas_len=0), dict(canvas_len=2048), dict(vocab=1),
                 dict(logits_dtype=7), dict(logits_ld=999), dict(entropy_budget=-1.0),
                 dict(entropy_budget=float("inf")), dict(conf_threshold=float("nan")),
-                dict(stable_k=0), dict(step_cap=0)):
+                dict(stable_k=0), dict(step_cap=0), dict(softcap=-1.0),
+                dict(softcap=float("nan")), dict(softcap=float("inf")),
+                dict(embed_scale=-2.0), dict(embed_scale=float("nan"))):
         assert dg.dg_workspace_bytes(_params(**bad), 0) == 0, bad
     assert L.dg_workspace_bytes(None, 0) == 0
 

@@ -6,6 +6,7 @@ times:
   position and every self-conditioning row;
 * 8 canvases x 256, V = 262144, bf16, d = 2816: one full canvas (acceptance
   and re-noise included), 64 random positions, 8 self-conditioning rows;
+* the same with the logit softcap (c = 30) and the sqrt(d) embedding scale;
 * 128 canvases x 256 (17 GB of logits): one full canvas, 64 random positions,
   4 self-conditioning rows;
 * the mixed-phase loop (32 requests: 8 prefill, 20 denoise, 4 commit) at
@@ -62,10 +63,12 @@ def _selfcond_rows(out, host_logits, rows, T, E_host, C):
         selfcond_check(out[q:q + 1], ref)
 
 
-def _one_step(B, C, V, dt, T, budget, d, boost, seed, n_rand, n_sc, full_canvas=True):
+def _one_step(B, C, V, dt, T, budget, d, boost, seed, n_rand, n_sc, full_canvas=True,
+              softcap=0.0, embed_scale=0.0):
     tdt = torch.bfloat16 if dt == dg.DG_BF16 else torch.float32
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dt, seed=seed,
-                  entropy_budget=budget, conf_threshold=0.3, stable_k=3, step_cap=32)
+                  entropy_budget=budget, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  softcap=softcap, embed_scale=embed_scale)
     st = make_state(p, [dg.DG_PHASE_DENOISE] * B, request_ids=np.arange(B) * 3 + 1,
                     temperatures=[T] * B, rng_step=np.arange(B))
     logits = syn.boosted_logits(B * C, V, seed=seed, dtype=tdt, device="cuda",
@@ -97,7 +100,8 @@ def _one_step(B, C, V, dt, T, budget, d, boost, seed, n_rand, n_sc, full_canvas=
     got = out.cpu().numpy()
     for q in sc_rows:
         ref = osc.selfcond_rows(L2[q:q + 1].float().cpu().numpy().astype(np.float64),
-                                float(after["temperature"][q // C]), E_host)
+                                float(after["temperature"][q // C]), E_host,
+                                cap=float(np.float32(softcap)), scale=float(np.float32(embed_scale)))
         selfcond_check(got[q:q + 1], ref)
 
 
@@ -126,6 +130,12 @@ def test_one_canvas_V50257_fp32_everything():
 
 def test_eight_canvases_V262144_bf16_sampled():
     _one_step(8, 256, 262144, dg.DG_BF16, 0.8, 96.0, 2816, 16.0, 0xD1FF0002, 64, 8)
+
+
+def test_eight_canvases_softcap_and_embed_scale_sampled():
+    # the softcapped path (c = 30) with the sqrt(d) embedding scale on the feed
+    _one_step(8, 256, 262144, dg.DG_BF16, 0.8, 96.0, 2816, 16.0, 0xD1FF0005, 64, 8,
+              softcap=30.0, embed_scale=float(np.sqrt(2816.0)))
 
 
 def test_128_canvases_V262144_bf16_sampled():
