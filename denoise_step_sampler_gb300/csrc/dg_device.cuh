@@ -126,13 +126,12 @@ __host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V
   // Gumbel screen, the first rounds' exact evaluations) is amortised over its
   // chunk, and a count that divides 8 keeps the eight warps of a CTA on whole
   // positions, so they share each position's screening bound.  The counts
-  // follow timings of the pass on a GB300 (152 SMs x 4 CTAs x 8 warps
-  // resident) at V = 262,144: 8 chunks for up to ~1,200 positions, 4 up to
-  // ~9,700, 2 beyond; never below 2048 logits per chunk.
-  const int64_t resident = 152 * 4 * 8;
+  // follow timings of the pass on a GB300 at V = 262,144 for 256 to 32,768
+  // positions (2, 4, 8 and 16 chunks tried at each): 8 chunks for up to 1,216
+  // positions, 4 up to 9,728, 2 beyond; never below 2048 logits per chunk.
   int64_t nc = 2;
-  if (n_pos * 4 <= 8 * resident) nc = 4;
-  if (n_pos * 8 <= 2 * resident) nc = 8;
+  if (n_pos <= 9728) nc = 4;
+  if (n_pos <= 1216) nc = 8;
   while (nc > 1 && ((int64_t)V + nc - 1) / nc < 2048) nc >>= 1;
   int64_t chunk = ((int64_t)V + nc - 1) / nc;
   chunk = (chunk + 255) / 256 * 256;

@@ -103,6 +103,24 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   L.m2 = m2n;
 }
 
+// Rounds of the bf16 path stream through a per-warp ring in shared memory
+// (cp.async, bypassing L1): while a warp works on round r, rounds r+1 and
+// r+2 are in flight, without holding registers.
+constexpr int kStages = 3;
+constexpr int kRingBytes = kWarps * kStages * 128 * 16;  // 48 KB per CTA
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -456,8 +474,10 @@ __device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32
 // CAP: logits pass through the softcap (cap_k = 2 log2(e) / c, cap_c = c)
 // before any other use; capped calls take the per-group path.
 template <int DT, bool CAP>
-// 4 CTAs of 8 warps per SM: the register budget is capped at 64 per thread
-__global__ void __launch_bounds__(kWarps * 32, 4)
+// The bf16 ring path runs 3 CTAs of 8 warps per SM (the ring and the queues
+// fill shared memory), at most 80 registers per thread; the other paths 4 CTAs
+// at 64.
+__global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
     vocab_pass_kernel(const void *__restrict__ logits, int64_t ld, int32_t V, int32_t C,
                       int64_t n_pos, int32_t chunk, int32_t n_chunks, uint64_t seed,
                       float cap_k, float cap_c,
@@ -466,6 +486,7 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
                       Partial *__restrict__ part, uint32_t *__restrict__ status) {
   __shared__ int32_t s_bound[kWarps];  // best score per position handled by this CTA
   __shared__ QEntry s_queue[kWarps][kQueue];
+  extern __shared__ uint4 s_ring[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   if (lane == 0) s_bound[warp] = f2ord(-INFINITY);
@@ -570,11 +591,32 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
       for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
       share_bound(slot, wb, lane);
     }
+    uint4 *ring = s_ring + (size_t)(threadIdx.x >> 5) * (kStages * 128);
+#pragma unroll
+    for (int r = 0; r < kStages - 1; ++r) {
+      if (r < rounds) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          cp_async16(ring + r * 128 + lane + u * 32, vrow + r * 128 + lane + u * 32);
+      }
+      cp_async_commit();
+    }
     for (int rd = 0; rd < rounds; ++rd) {
       const int q = rd * 128 + lane;
+      {
+        const int r = rd + kStages - 1;
+        if (r < rounds) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            cp_async16(ring + (r % kStages) * 128 + lane + u * 32, vrow + r * 128 + lane + u * 32);
+        }
+        cp_async_commit();
+      }
+      cp_async_wait<kStages - 1>();
+      const uint4 *cur = ring + (rd % kStages) * 128;
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = ld_stream(vrow + q + u * 32);
+      for (int u = 0; u < 4; ++u) v[u] = cur[lane + u * 32];
       const float rmax = round_max_bf16(v);
       if (rmax > L.zmax) am_round = rd;
       L.zmax = fmaxf(L.zmax, rmax);
@@ -607,19 +649,20 @@ __global__ void __launch_bounds__(kWarps * 32, 4)
 #pragma unroll
       for (int u = 0; u < 4; ++u) any |= fmix32(K.ka ^ (gq + 32u * u)) >= lim;
       if (__any_sync(0xFFFFFFFFu, any)) {
-        // rare: reload the round (L2) and queue the passing groups
+        // rare: reread the round from the ring and queue the passing groups
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const uint32_t g = gq + 32u * u;
           const uint32_t h = fmix32(K.ka ^ g);
           float z[8];
-          unpack_bf16x8(ld_stream(vrow + q + u * 32), z);
+          unpack_bf16x8(cur[lane + u * 32], z);
           coop_eval(h >= lim, z, g, h, c, wb, K, L, lane, Q);
         }
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
     }
+    cp_async_wait<0>();
     if (am_round >= 0) {
       // lowest index holding the lane's maximum, in the round that set it
       const int q = am_round * 128 + lane;
@@ -748,11 +791,23 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const int64_t warps = n_pos * n_chunks;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  {
+    static bool attr_set[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    }
+  }
   const bool cap = p.softcap > 0.f;
   const float cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
   const float cap_c = cap ? p.softcap : 0.f;
 #define DG_VOCAB_LAUNCH(DT, CAP)                                                              \
-  vocab_pass_kernel<DT, CAP><<<(unsigned)blocks, kWarps * 32, 0, s>>>(                        \
+  vocab_pass_kernel<DT, CAP><<<(unsigned)blocks, kWarps * 32, (DT == DG_BF16 && !CAP) ? kRingBytes : 0, s>>>( \
       logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c, \
       st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status)
   if (p.logits_dtype == DG_BF16) {
