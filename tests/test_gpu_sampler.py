@@ -38,6 +38,11 @@ CASES = [
     (2, 64, 50257, dg.DG_BF16, 50264, 30.0, [0.9, 1.1]),        # aligned bf16 rows, ragged V
     (2, 32, 4099, dg.DG_BF16, 4099, 20.0, [1.2, 0.6]),          # 2-byte aligned bf16 rows
     (1, 100, 2048, dg.DG_F32, None, 5.0, [1.0]),                # C not a power of two
+    (1, 8, 8192, dg.DG_BF16, None, 2.0, [0.9]),                 # one bf16 round per chunk
+    (1, 8, 16384, dg.DG_BF16, None, 2.0, [0.9]),                # two rounds (fewer than the ring)
+    (1, 16, 2, dg.DG_F32, None, 1.0, [1.0]),                    # smallest vocabulary
+    (3, 1, 300, dg.DG_BF16, None, 0.5, [0.8, 1.0, 1.2]),        # one position per canvas
+    (1, 1024, 4096, dg.DG_BF16, None, 300.0, [1.0]),            # largest canvas
 ]
 
 

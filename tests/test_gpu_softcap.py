@@ -47,8 +47,16 @@ def test_softcap_step_matches_oracle(case):
     tdt = torch.bfloat16 if dt == dg.DG_BF16 else torch.float32
     logits = syn.boosted_logits(B * C, V, seed=V + int(cap), dtype=tdt, device="cuda", ld=ld,
                                 boost_hi=24.0).reshape(-1)
+    st2 = make_state(p, [dg.DG_PHASE_DENOISE] * B, request_ids=np.arange(B) + 5,
+                     temperatures=np.linspace(0.7, 1.2, B))
     _, after, _, _, _ = denoise_and_compare(p, st, logits)
     assert after["device_status"][0] == 0
+    # the allocation-free entry runs the same capped kernels
+    dg.dg_denoise_step_noalloc(p, logits, st2)
+    torch.cuda.synchronize()
+    b = st2.snapshot()
+    for k in after:
+        assert np.array_equal(after[k], b[k], equal_nan=after[k].dtype.kind == "f"), k
 
 
 def test_softcap_infinite_and_nan_logits():
