@@ -1,11 +1,12 @@
 // K2 -- one CTA per request slot: the per-canvas half of the sampler step.
 //
 // DENOISE rows: merge the vocabulary-pass partials of each position into
-// (m, s, H, argmax, cand); then, under the entropy-budget rule, sort the
-// canvas's (H, i) pairs ascending with a bitonic network in shared memory,
-// take the exclusive prefix sum of the sorted entropies in fp64 and accept
-// while it stays within the budget (the first always) -- "DiffusionGemma
-// Explained", section "Sampling", step 3; re-noise rejected positions to
+// (m, s, H, argmax, cand); then, under the entropy-budget rule, accept the
+// positions of the ascending (H, i) order while the exclusive prefix sum of
+// their entropies stays within the budget (the first always) -- "DiffusionGemma
+// Explained", section "Sampling", step 3.  The order is never materialised:
+// each position counts the pairs ranked before it and sums their entropies
+// in 2^-40 fixed point (exact integer sums).  Re-noise rejected positions to
 // uniform tokens (Technical Report section 3.3).  Under the monotone rule
 // ("DiffusionGemma-Lite DIFFUSION.html", section 4.2) each position commits
 // on an unchanged argmax or a confidence 1/s no lower than the last step's,
@@ -23,20 +24,15 @@ namespace {
 
 constexpr int kMaxC = 1024;
 
-__device__ __forceinline__ double warp_incl_scan(double x, int lane) {
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const double y = __shfl_up_sync(0xFFFFFFFFu, x, off);
-    if (lane >= off) x += y;
-  }
-  return x;
-}
-
-__device__ __forceinline__ double warp_sum(double x) {
+__device__ __forceinline__ long long warp_sum(long long x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
   return x;
 }
+
+// An entropy in 2^-40 fixed point: exact for every fp32 value >= 2^-16, so
+// sums of a canvas's entropies are exact integer sums.
+__device__ __forceinline__ long long hfix(float h) { return __float2ll_rn(h * 0x1p40f); }
 
 struct CanvasArgs {
   int32_t B, C, V;
@@ -54,10 +50,8 @@ struct CanvasArgs {
 
 __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
   __shared__ float skey[kMaxC];
-  __shared__ int32_t sidx[kMaxC];
-  __shared__ uint8_t sacc[kMaxC];
-  __shared__ double swarp[32];
-  __shared__ double soff[32];
+  __shared__ long long sfix[kMaxC];
+  __shared__ long long swarp[32];
   __shared__ float sH[kMaxC], sS[kMaxC];
   __shared__ int32_t sAm[kMaxC], sCand[kMaxC];
 
@@ -199,8 +193,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       bool ok = !(fl & (kPartNaN | kPartPInf | kPartBadT)) && zmax != -INFINITY && pam >= 0 &&
                 pcand >= 0 && S > 0.f && isfinite(S) && isfinite(Tt);
       float Hf = NAN, m_out = NAN, s_out = NAN;
-      if (ok) {
-        Hf = (float)(0.6931471805599453 * (log2((double)S) - (double)Tt / (double)S));
+      if (ok) {  // S >= 1 (the maximum contributes 2^0); fp32 keeps H within ~1e-6
+        Hf = 0.69314718f * (log2f(S) - __fdiv_rn(Tt, S));
         m_out = zmax / T;
         s_out = S;
       } else if (!(fl & kPartBadT)) {
@@ -225,7 +219,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
 
   const int32_t step0 = st.step[r];
   int same = 1;
-  double hsum = 0.0;
+  long long hsum = 0;  // this position's entropy in fixed point (valid ones)
+  bool bad = false;    // an invalid position makes the mean NaN
   if (monotone) {
     if (tid < C) {
       const int32_t prev_am = st.argmax_prev[base + tid];
@@ -249,55 +244,37 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       st.accept[base + tid] = nw ? 1 : 0;
       same = (prev_am == am) ? 1 : 0;
       st.argmax_prev[base + tid] = am;
-      hsum = valid ? (double)H : (double)NAN;
+      hsum = valid ? hfix(H) : 0;
+      bad = !valid;
     }
   } else {
-    // sort (H, i) ascending; invalid positions and padding sort last as +inf
-    skey[tid] = valid ? H : INFINITY;
-    sidx[tid] = tid;
+    // rank (H, i) ascending among the canvas (invalid positions last, as
+    // +inf) and sum the entropies ranked before each position
+    const float key = valid ? H : INFINITY;
+    if (tid < C) {
+      skey[tid] = key;
+      sfix[tid] = valid ? hfix(key) : 0;
+    }
     __syncthreads();
-    for (int k = 2; k <= nt; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const int o = tid ^ j;
-        if (o > tid) {
-          const float ka = skey[tid], kb = skey[o];
-          const int32_t ia = sidx[tid], ib = sidx[o];
-          const bool gt = (ka > kb) || (ka == kb && ia > ib);
-          const bool up = ((tid & k) == 0);
-          if (gt == up) {
-            skey[tid] = kb;
-            skey[o] = ka;
-            sidx[tid] = ib;
-            sidx[o] = ia;
-          }
+    bool acc_me = false;
+    if (tid < C && valid) {
+      long long before = 0;  // entropies ranked before this position
+      bool first = true;     // nothing ranked before it
+      for (int j = 0; j < C; ++j) {  // every thread reads the same word: a broadcast
+        const float kj = skey[j];
+        if (kj < key || (kj == key && j < tid)) {
+          first = false;
+          before += sfix[j];
         }
-        __syncthreads();
       }
+      const float bf = a.budget * 0x1p40f;  // the budget in the same fixed point
+      const long long bfix = bf >= 0x1p62f ? 0x3FFFFFFFFFFFFFFFll : __float2ll_rd(bf);
+      acc_me = first || before <= bfix;
     }
-
-    // exclusive prefix sum of the sorted entropies (fp64), then the budget rule
-    const double x = (double)skey[tid];
-    const double incl = warp_incl_scan(x, lane);
-    double excl = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
-    if (lane == 0) excl = 0.0;
-    if (lane == 31) swarp[warp] = incl;
-    __syncthreads();
-    if (tid == 0) {
-      double run = 0.0;
-      for (int w = 0; w < nwarps; ++w) {
-        soff[w] = run;
-        run += swarp[w];
-      }
-    }
-    __syncthreads();
-    const double E = soff[warp] + excl;
-    const bool acc_k = isfinite(x) && (tid == 0 || E <= (double)a.budget);
-    sacc[sidx[tid]] = acc_k ? 1 : 0;
-    __syncthreads();
 
     // re-noise, accept mask
     if (tid < C) {
-      const bool acc = sacc[tid] != 0;
+      const bool acc = acc_me;
       st.accept[base + tid] = acc ? 1 : 0;
       int32_t tok = cand;
       if (!acc) {
@@ -307,18 +284,20 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       st.canvas[base + tid] = tok;
       same = (st.argmax_prev[base + tid] == am) ? 1 : 0;
       st.argmax_prev[base + tid] = am;
-      hsum = valid ? (double)H : (double)NAN;
+      hsum = valid ? hfix(H) : 0;
+      bad = !valid;
     }
   }
   // convergence
   const int all_same = __syncthreads_and(same);
-  const double wsum = warp_sum(hsum);
+  const int any_bad = __syncthreads_or(bad);
+  const long long wsum = warp_sum(hsum);
   if (lane == 0) swarp[warp] = wsum;
   __syncthreads();
   if (tid == 0) {
-    double tot = 0.0;
+    long long tot = 0;
     for (int w = 0; w < nwarps; ++w) tot += swarp[w];
-    const double hbar = tot / (double)C;
+    const double hbar = any_bad ? (double)NAN : (double)tot * 0x1p-40 / (double)C;
     const int32_t step1 = step0 + 1;
     int32_t stable;
     bool conv;
