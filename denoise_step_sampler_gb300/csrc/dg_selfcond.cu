@@ -33,20 +33,23 @@ namespace {
 constexpr int BM = 256;  // rows per CTA: two M=128 MMAs share every E tile
 constexpr int BN = 256;  // embedding columns per CTA (one N=256 MMA per row half)
 constexpr int BK = 64;   // one 128-byte swizzle row of bf16
-constexpr int NST = 3;   // stages of 64 KB
+// Two operand rings that advance separately: E tiles (mostly from DRAM, the
+// slow ones to land) run one stage deeper than the logits tiles, which also
+// wait for the p rebuild.
+constexpr int NE = 4;    // E stages of 32 KB
+constexpr int NA = 3;    // logits / p stages of 32 KB
 constexpr int kProdWarps = 16;  // four per scheduler: the p rebuild is latency-bound
-constexpr int kAIssuers = 2;  // TMA warps that also load one 128-row half of the logits tile
+constexpr int kAIssuers = 2;  // TMA warps that each load one 128-row half of the logits tile
 constexpr int kFirstAWarp = 2 + kProdWarps;
-// warp 0 E-tile TMA, warp 1 MMA, 16 producer/epilogue warps, 2 logits-and-E
-// TMA warps (20 warps: a multiple of 4, so the register cap is 96)
+// warp 0 E-tile TMA, warp 1 MMA, 16 producer/epilogue warps, 2 logits TMA
+// warps (20 warps: a multiple of 4, so the register cap is 96)
 constexpr int kThreads = 32 * (kFirstAWarp + kAIssuers);
-constexpr int kTmaWarps = 1 + kAIssuers;  // E boxes are dealt round-robin over these
 constexpr uint32_t kABytes = BM * BK * 2;  // 32 KB
 constexpr uint32_t kAHalf = 128 * BK * 2;  // 16 KB: one M=128 operand
 constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 64 rows x 128 B
 constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
 constexpr uint32_t kSharedBytes = 1024;  // barriers + per-row flags, after the stages
-constexpr uint32_t kSmemBytes = NST * (kABytes + kBBytes) + kSharedBytes + 1024;  // + alignment
+constexpr uint32_t kSmemBytes = NE * kBBytes + NA * kABytes + kSharedBytes + 1024;  // + alignment
 static_assert(kSmemBytes <= 232448, "over the 227 KB per-CTA shared memory limit");
 constexpr int kAssumedSMs = 152;
 // E tiles come mostly from DRAM, logits tiles mostly from L2 (the column tiles
@@ -58,12 +61,12 @@ constexpr int kPrefetchKb = 4;
 #endif
 constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
 
-template <int NS>
-struct SharedT {
-  uint64_t full[NS];     // TMA bytes of the stage's E tile landed
-  uint64_t a_full[NS];   // TMA bytes of the stage's logits tile landed
-  uint64_t a_ready[NS];  // producers wrote p into the A tile
-  uint64_t empty[NS];    // the MMAs reading the stage completed
+struct Shared {
+  uint64_t full[NE];     // TMA bytes of the stage's E tile landed
+  uint64_t empty[NE];    // the MMAs reading the E stage completed (every CTA of the cluster)
+  uint64_t a_full[NA];   // TMA bytes of the stage's logits tile landed
+  uint64_t a_ready[NA];  // producers wrote p into the A tile
+  uint64_t a_empty[NA];  // the MMAs reading the A stage completed
   uint64_t tmem_full;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -71,7 +74,6 @@ struct SharedT {
   int32_t any_valid;
   uint8_t row_ok[BM];
 };
-using Shared = SharedT<NST>;
 static_assert(sizeof(Shared) <= kSharedBytes, "barrier block outgrew its reservation");
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -108,7 +110,7 @@ __device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
 // First wait that gave up since load (diagnostics): {set, block, where, parity}.
 // where = role << 28 | barrier << 24 | stage << 16 | k-iteration (low 16 bits);
 // roles 0 TMA, 1 MMA, 2 producer, 3 epilogue; barriers 0 full, 1 a_ready,
-// 2 empty, 3 tmem_full.
+// 2 empty (E), 3 tmem_full, 4 a_full, 5 a_empty.
 __device__ uint32_t g_wait_record[4];
 
 namespace {
@@ -118,7 +120,7 @@ __device__ __forceinline__ uint32_t where_code(uint32_t role, uint32_t bar, int 
 }
 
 // Bounded wait; false if it gave up or another role aborted.
-__device__ __noinline__ bool mbar_wait_flag(uint64_t *b, uint32_t parity, int32_t *abort_flag,
+__device__ __forceinline__ bool mbar_wait_flag(uint64_t *b, uint32_t parity, int32_t *abort_flag,
                                             uint32_t *status, uint32_t where) {
   // Poll the barrier; only every 256th failed poll looks at the abort flag and
   // the clock, so a completed phase is noticed at once.
@@ -421,9 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t *sB = smem;                   // NST x 16 KB (1024-aligned)
-  uint8_t *sA = smem + NST * kBBytes;   // NST x 16 KB
-  Shared *sh = reinterpret_cast<Shared *>(smem + NST * (kABytes + kBBytes));
+  uint8_t *sB = smem;                  // NE x 32 KB (1024-aligned)
+  uint8_t *sA = smem + NE * kBBytes;   // NA x 32 KB
+  Shared *sh = reinterpret_cast<Shared *>(smem + NE * kBBytes + NA * kABytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (CL > 1) ? (int)cluster_rank() : 0;
@@ -442,11 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes;  // E bytes landing in this CTA
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
+    for (int s = 0; s < NE; ++s) {
       mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], CL);  // one MMA-commit arrival from each CTA of the cluster
+    }
+    for (int s = 0; s < NA; ++s) {
       mbar_init(&sh->a_full[s], kAIssuers);
       mbar_init(&sh->a_ready[s], kProdWarps);
-      mbar_init(&sh->empty[s], CL);  // one MMA-commit arrival from each CTA of the cluster
+      mbar_init(&sh->a_empty[s], 1);  // this CTA's MMA commit
     }
     mbar_init(&sh->tmem_full, 1);
     mbar_init(&sh->mma_done, 1);
@@ -479,39 +484,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool run = any != 0 && nkb > 0;
 
   if (run) {
-    if (warp == 0 || warp >= kFirstAWarp) {
-      // ------------------------------------------------ TMA
-      // TMA warp tw (0: warp 0; 1, 2: the logits warps) loads the logits half
-      // tw - 1 (tw >= 1) and the E boxes j with j % CL == rank (multicast to
-      // the cluster when CL > 1) whose index among this CTA's boxes is tw
-      // modulo kTmaWarps.  Warp 0 alone posts the stage's expected E bytes
-      // (all boxes, own and peers').
-      const int tw = (warp == 0) ? 0 : 1 + (warp - kFirstAWarp);
-      const bool do_a = a.tma_a && tw >= 1;
-      int mine = 0;
-      for (int j = rank; j < n_box; j += CL) mine += ((j / CL) % kTmaWarps) == tw;
-      const bool prefetch = tw == 0 && rank == 0;
-      if (lane == 0 && (do_a || mine > 0 || tw == 0)) {
+    if (warp == 0) {
+      // ------------------------------------------------ E ring (TMA)
+      // Warp 0 posts the stage's expected E bytes (all boxes, own and peers')
+      // and loads the boxes j with j % CL == rank, multicast to the cluster
+      // when CL > 1; one CTA per cluster also prefetches E into L2.
+      const bool prefetch = rank == 0;
+      if (lane == 0) {
         if (prefetch)
           for (int i = 0; i < min(kPrefetchKb, nkb); ++i)
             tma_prefetch_2d(&tmap_ep, n0, (kb0 + i) * BK);
         int issued = 0;
         for (int i = 0; i < nkb; ++i) {
-          const int s = i % NST;
-          const uint32_t use = (uint32_t)(i / NST);
-          if (i >= NST &&
+          const int s = i % NE;
+          const uint32_t use = (uint32_t)(i / NE);
+          if (i >= NE &&
               !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
             break;
           const int32_t kv = (kb0 + i) * BK;
-          if (do_a) {
-            mbar_expect_tx(&sh->a_full[s], kAHalf);
-            tma_load_2d(sA + s * kABytes + (tw - 1) * kAHalf, &tmap_z, &sh->a_full[s], kv,
-                        (int32_t)(row0 + (tw - 1) * 128));
-          }
-          if (tw == 0) mbar_expect_tx(&sh->full[s], stage_tx);
+          mbar_expect_tx(&sh->full[s], stage_tx);
           uint8_t *dstB = sB + s * kBBytes;
           for (int j = rank; j < n_box; j += CL) {
-            if (((j / CL) % kTmaWarps) != tw) continue;
             if (CL == 1)
               tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
             else
@@ -523,21 +516,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = i + 1;
         }
         // every issued copy must land before the CTA may exit
-        for (int i = max(0, issued - NST); i < issued; ++i) {
-          mbar_drain(&sh->full[i % NST], (uint32_t)(i / NST) & 1u);
-          if (do_a) mbar_drain(&sh->a_full[i % NST], (uint32_t)(i / NST) & 1u);
+        for (int i = max(0, issued - NE); i < issued; ++i)
+          mbar_drain(&sh->full[i % NE], (uint32_t)(i / NE) & 1u);
+      }
+    } else if (warp >= kFirstAWarp) {
+      // ------------------------------------------------ logits ring (TMA)
+      // Warp kFirstAWarp + h loads the 128-row half h of the logits tile.
+      const int h = warp - kFirstAWarp;
+      if (lane == 0 && a.tma_a) {
+        int issued = 0;
+        for (int i = 0; i < nkb; ++i) {
+          const int s = i % NA;
+          const uint32_t use = (uint32_t)(i / NA);
+          if (i >= NA &&
+              !mbar_wait(&sh->a_empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 5, s, i)))
+            break;
+          mbar_expect_tx(&sh->a_full[s], kAHalf);
+          tma_load_2d(sA + s * kABytes + h * kAHalf, &tmap_z, &sh->a_full[s], (kb0 + i) * BK,
+                      (int32_t)(row0 + h * 128));
+          issued = i + 1;
         }
+        for (int i = max(0, issued - NA); i < issued; ++i)
+          mbar_drain(&sh->a_full[i % NA], (uint32_t)(i / NA) & 1u);
       }
     } else if (warp == 1) {
       // ------------------------------------------------ MMA issuer
       if (lane == 0) {
         for (int i = 0; i < nkb; ++i) {
-          const int s = i % NST;
-          const uint32_t par = (uint32_t)(i / NST) & 1u;
-          if (!mbar_wait(&sh->full[s], par, sh, a.status, where_code(1, 0, s, i))) break;
-          if (!mbar_wait(&sh->a_ready[s], par, sh, a.status, where_code(1, 1, s, i))) break;
+          const int s = i % NE, sa = i % NA;
+          if (!mbar_wait(&sh->full[s], (uint32_t)(i / NE) & 1u, sh, a.status,
+                         where_code(1, 0, s, i)))
+            break;
+          if (!mbar_wait(&sh->a_ready[sa], (uint32_t)(i / NA) & 1u, sh, a.status,
+                         where_code(1, 1, sa, i)))
+            break;
           tc_fence_after();
-          const uint32_t a_base = smem_u32(sA + s * kABytes);
+          const uint32_t a_base = smem_u32(sA + sa * kABytes);
           const uint32_t b_base = smem_u32(sB + s * kBBytes);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
@@ -551,7 +565,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (CL == 1)
             mma_commit(&sh->empty[s]);
           else
-            mma_commit_mc(&sh->empty[s], cl_mask);  // every CTA may now reuse stage s
+            mma_commit_mc(&sh->empty[s], cl_mask);  // every CTA may now reuse E stage s
+          mma_commit(&sh->a_empty[sa]);             // this CTA may reuse A stage sa
         }
         mma_commit(&sh->tmem_full);
         mma_commit(&sh->mma_done);
@@ -577,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 4; ++j) off[j] = a_off((t >> 3) + 64 * j, ch);
       if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
-          const int s = i % NST;
-          const uint32_t par = (uint32_t)(i / NST) & 1u;
+          const int s = i % NA;
+          const uint32_t par = (uint32_t)(i / NA) & 1u;
           // the whole warp leaves together if the wait gives up
           if (!__all_sync(0xFFFFFFFFu,
                           mbar_wait(&sh->a_full[s], par, sh, a.status, where_code(2, 4, s, i))))
@@ -632,11 +647,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((okm >> j) & 1u) x[j] = load_raw8(a, rowp + (size_t)j * jstride, k);
         }
         for (int i = 0; i < nkb; ++i) {
-          const int s = i % NST;
-          const uint32_t use = (uint32_t)(i / NST);
-          if (i >= NST &&
-              !__all_sync(0xFFFFFFFFu, mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status,
-                                                 where_code(2, 2, s, i))))
+          const int s = i % NA;
+          const uint32_t use = (uint32_t)(i / NA);
+          if (i >= NA &&
+              !__all_sync(0xFFFFFFFFu, mbar_wait(&sh->a_empty[s], (use - 1) & 1u, sh, a.status,
+                                                 where_code(2, 5, s, i))))
             break;
           uint8_t *tileA = sA + s * kABytes;
           const int64_t k = (int64_t)(kb0 + i) * BK + ch * 8;

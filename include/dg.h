@@ -240,8 +240,8 @@ int dg_denoise_step_noalloc(const dg_params *p, const void *logits, const dg_sta
  * GEMM that gave up since the library was loaded, as {set, block, where,
  * parity}; set = 0 if none did.  where = role << 28 | barrier << 24 |
  * stage << 16 | k-iteration (roles 0 TMA, 1 MMA, 2 producer, 3 epilogue;
- * barriers 0 E tile landed, 1 a_ready, 2 empty, 3 tmem_full, 4 logits tile
- * landed).  Synchronous; not for
+ * barriers 0 E tile landed, 1 a_ready, 2 E stage free, 3 tmem_full, 4 logits
+ * tile landed, 5 logits stage free).  Synchronous; not for
  * use inside a captured graph. */
 int dg_debug_wait_record(uint32_t out[4]);
 
