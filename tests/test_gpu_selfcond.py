@@ -44,6 +44,7 @@ CASES = [
     (5, 256, 1024, dg.DG_F32, None, 1024, 1024, torch.float32),  # fp32, many row tiles
     (2, 128, 5000, dg.DG_BF16, 5008, 256, 256, torch.float32),   # bf16 by TMA, ld > V, ragged k
     (2, 96, 3001, dg.DG_BF16, 3003, 208, 208, torch.bfloat16),   # bf16 rows not 16-byte aligned
+    (4, 256, 4096, dg.DG_BF16, None, 400, 400, torch.float32),   # clusters of 2, 3 E boxes in the last column tile
     (3, 1, 300, dg.DG_BF16, None, 16, 16, torch.float32),        # one position per canvas
     (1, 16, 2, dg.DG_F32, None, 32, 32, torch.float32),          # smallest vocabulary
 ]
