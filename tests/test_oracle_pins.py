@@ -620,3 +620,19 @@ def test_selfcond_softcap_and_scale_by_hand():
                                                  cap=5.0, scale=1.0))
     assert np.allclose(selfcond.selfcond(L, np.ones(2), E2, np.array([True, True]), cap=5.0,
                                          scale=3.5), 3.5 * one, rtol=1e-15, atol=0)
+
+
+def test_softcap_large_c_reduces_to_the_uncapped_step():
+    # c tanh(z / c) -> z as c grows: with |z| <= ~20 and c = 1e6 the cap moves
+    # each logit by < z^3 / (3 c^2) ~ 3e-9, so the step is unchanged
+    g = np.random.default_rng(24)
+    C, V = 8, 50
+    z = g.normal(0, 4, (1, C, V))
+    base = dict(batch=1, canvas_len=C, vocab=V, seed=91, entropy_budget=6.0,
+                conf_threshold=0.3, stable_k=2, step_cap=8)
+    st = sampler.new_state(sampler.Params(**base), [sampler.PHASE_DENOISE], [7], [0.8])
+    a, _ = sampler.step(sampler.Params(**base, softcap=1e6), st, z)
+    b, _ = sampler.step(sampler.Params(**base), st, z)
+    for k in ("canvas", "cand", "argmax", "accept"):
+        assert np.array_equal(getattr(a, k), getattr(b, k)), k
+    assert np.allclose(a.entropy, b.entropy, rtol=0, atol=1e-7)
