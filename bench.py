@@ -358,9 +358,7 @@ def run_ours(args, rank, world, dev):
     sc_tflops = flops / (ms_sc / 1e3) / 1e12
     logit_bytes = n_pos * V * esz
     sampler_gbs = logit_bytes / (ms_sampler / 1e3) / 1e9
-    from denoise_step_sampler_gb300 import build as _b  # noqa: F401
-    plan_splits = _selfcond_splits(n_pos, V, d)
-    launches_per_step = 2 + 1 + (1 if plan_splits > 1 else 0)
+    launches_per_step = 2 + _selfcond_launches(p, d)
     line = {
         "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K,
@@ -409,23 +407,13 @@ def run_ours(args, rank, world, dev):
     return line
 
 
-def _selfcond_splits(rows, V, d):
-    # mirrors the library's split plan only to count launches (no effect on timing)
-    BM, BN, BK, SMS = 256, 256, 64, 152
-    m, n, k = -(-rows // BM), -(-d // BN), -(-V // BK)
-    cl = 2 if m >= 2 else 1
-    tiles = -(-m // cl) * cl * n
-    best, best_eff = 1, 0.0
-    for sp in range(1, 65):
-        if sp > 1 and k // sp < 16:
-            break
-        ctas = tiles * sp
-        waves = -(-ctas // SMS)
-        eff = m * n * sp / (waves * SMS)
-        if eff > best_eff + 0.05:
-            best, best_eff = sp, eff
-    kbps = -(-k // best)
-    return -(-k // kbps)
+def _selfcond_launches(p, d):
+    """Kernel launches of one dg_selfcond_embed call: the GEMM, plus the
+    split-K reduction when the library splits the vocabulary, which it does
+    exactly when the self-conditioning needs more workspace than the sampler
+    (its fp32 partial sums are [splits][rows][d])."""
+    import denoise_step_sampler_gb300 as dg
+    return 2 if dg.dg_workspace_bytes(p, d) > dg.dg_workspace_bytes(p, 0) else 1
 
 
 def run_graph_loop(args, dev):

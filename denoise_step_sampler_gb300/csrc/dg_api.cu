@@ -1,6 +1,7 @@
 // C-ABI front end: argument validation (no side effect on failure), the
 // workspace query, and the launches of the sampler kernels on the caller's
 // stream.  Nothing here allocates, frees or synchronises.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -8,9 +9,7 @@
 #include "dg_device.cuh"
 #include "dg_internal.h"
 
-using namespace dg;
-
-namespace {
+namespace dg {
 
 bool params_ok(const dg_params *p) {
   if (!p) return false;
@@ -34,12 +33,34 @@ bool params_ok(const dg_params *p) {
 
 bool aligned(const void *ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
 
+namespace {
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
 
 size_t denoise_ws_bytes(const dg_params *p) {
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
   const VocabChunking vc = vocab_chunking(n_pos, p->vocab);
   return round_up((size_t)n_pos * (size_t)vc.n_chunks * sizeof(Partial), 256);
+}
+
+int32_t device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  static std::atomic<int32_t> cache[64];  // 0 = not yet queried
+  if (dev >= 0 && dev < 64) {
+    const int32_t c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 // The device must be an sm_103 part (GB300); checked once per device.
@@ -49,8 +70,11 @@ int device_ok() {
     cudaGetLastError();
     return DG_ERR_CUDA;
   }
-  static int cache[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
-  if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev] == 1 ? DG_OK : DG_ERR_UNSUPPORTED;
+  static std::atomic<int> cache[64];  // 0 unknown, 1 ok, 2 unsupported
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c) return c == 1 ? DG_OK : DG_ERR_UNSUPPORTED;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -58,7 +82,7 @@ int device_ok() {
     return DG_ERR_CUDA;
   }
   const bool ok = (major == 10 && minor == 3);
-  if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+  if (dev >= 0 && dev < 64) cache[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   return ok ? DG_OK : DG_ERR_UNSUPPORTED;
 }
 
@@ -79,7 +103,17 @@ bool rule_state_ok(const dg_params *p, const dg_state *st) {
   return p->accept_rule != DG_ACCEPT_MONOTONE || (st->committed && st->prev_conf);
 }
 
-}  // namespace
+int denoise_args_ok(const dg_params *p, const void *logits, const dg_state *st) {
+  if (!params_ok(p) || !state_ok_full(st) || !logits || !rule_state_ok(p, st))
+    return DG_ERR_INVALID_ARG;
+  const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
+  if (!aligned(logits, esz)) return DG_ERR_INVALID_ARG;
+  return DG_OK;
+}
+
+}  // namespace dg
+
+using namespace dg;
 
 extern "C" {
 
@@ -87,7 +121,8 @@ size_t dg_workspace_bytes(const dg_params *p, int32_t d) {
   if (!params_ok(p) || d < 0) return 0;
   size_t ws = denoise_ws_bytes(p);
   if (d > 0) {
-    const SelfcondPlan pl = selfcond_plan((int64_t)p->batch * p->canvas_len, p->vocab, d);
+    const SelfcondPlan pl =
+        selfcond_plan((int64_t)p->batch * p->canvas_len, p->vocab, d, device_sm_count());
     if (pl.ws_bytes > ws) ws = pl.ws_bytes;
   }
   return ws;
@@ -137,10 +172,8 @@ int dg_anneal_temperature(const dg_params *p, const int32_t *step, float *temper
 
 int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st, void *ws,
                     size_t ws_bytes, cudaStream_t stream) {
-  if (!params_ok(p) || !state_ok_full(st) || !logits || !rule_state_ok(p, st))
-    return DG_ERR_INVALID_ARG;
-  const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
-  if (!aligned(logits, esz)) return DG_ERR_INVALID_ARG;
+  const int rc = denoise_args_ok(p, logits, st);
+  if (rc != DG_OK) return rc;
   const size_t need = denoise_ws_bytes(p);
   if (!ws || ws_bytes < need || !aligned(ws, 16)) return DG_ERR_WORKSPACE;
   const int dv = device_ok();
@@ -167,7 +200,7 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
   const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
   if (!aligned(logits, esz) || !aligned(E, 16) || !aligned(out, 16)) return DG_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)p->batch * p->canvas_len;
-  const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d);
+  const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d, device_sm_count());
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned(ws, 16)))
     return DG_ERR_WORKSPACE;
   const int dv = device_ok();

@@ -12,6 +12,21 @@ namespace dg {
 
 struct Partial;
 
+// Host-side argument checks shared by the entry points (dg_api.cu).  None has
+// a side effect.
+bool params_ok(const dg_params *p);             // sizes, enums, finite scalars
+bool aligned(const void *ptr, size_t a);
+bool state_ok_phase_machine(const dg_state *st);  // arrays the phase machine writes
+bool state_ok_full(const dg_state *st);           // every array of a denoise step
+bool rule_state_ok(const dg_params *p, const dg_state *st);  // monotone-rule arrays
+// Every check of dg_denoise_step that precedes its workspace check:
+// DG_OK or DG_ERR_INVALID_ARG.
+int denoise_args_ok(const dg_params *p, const void *logits, const dg_state *st);
+// Bytes of partial records the vocabulary pass writes for these sizes.
+size_t denoise_ws_bytes(const dg_params *p);
+// DG_OK on an sm_103 device, else DG_ERR_UNSUPPORTED or DG_ERR_CUDA.
+int device_ok();
+
 // K1: fused vocabulary pass -> per (position, chunk) partial records.
 cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_state &st,
                               Partial *part, int32_t chunk, int32_t n_chunks, cudaStream_t s);
@@ -24,16 +39,20 @@ cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Par
 
 // K4: self-conditioning GEMM (tcgen05 / TMEM).
 struct SelfcondPlan {
-  int32_t m_tiles;   // ceil(B*C / 128)
+  int32_t m_tiles;   // ceil(B*C / BM)
   int32_t n_tiles;   // ceil(d / BN)
   int32_t splits;    // K splits over the vocabulary
   int32_t k_blocks;  // ceil(V / BK)
   int32_t kb_per_split;  // k-blocks per split (every split non-empty)
-  int32_t cluster;   // CTAs per cluster sharing E tiles by multicast (1, 2 or 4)
-  int32_t m_groups;  // ceil(m_tiles / cluster)
+  int32_t n_sms;     // SMs the plan fills in whole waves
   size_t ws_bytes;   // split-K partial sums (0 if splits == 1)
 };
-SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d);
+// The split count depends on the sizes and on the number of SMs (n_sms).
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms);
+
+// SMs of the current device (cached per device); 152, the GB300's count, when
+// no device can be queried (host-only callers of the workspace query).
+int32_t device_sm_count();
 cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                             void *ws, const SelfcondPlan &plan, cudaStream_t s);

@@ -12,7 +12,10 @@
 // call's contents; nothing needs clearing, because the vocabulary pass writes
 // every record that the canvas kernel later reads.  Two calls whose kernels
 // overlap on the GPU (different streams, no ordering) race on the array.
+#include <cuda.h>
+
 #include <cstdint>
+#include <mutex>
 
 #include "dg_device.cuh"
 #include "dg_internal.h"
@@ -22,11 +25,33 @@ namespace {
 constexpr size_t kScratchRecords = 65536;  // 2 MiB of 32-byte partial records
 static __device__ __align__(256) dg::Partial g_noalloc_scratch[kScratchRecords];
 
-// Device address of the array, looked up once per device.  In host code the
-// array's name is only a host-side stand-in, so its device address comes
-// from cudaGetSymbolAddress with that device current.
+// Device address of the array, looked up once per device with that device
+// current (in host code the array's name is only a host-side stand-in).  A
+// context created after cudaDeviceReset loads the module again, possibly at
+// another address, so each entry remembers the context it was looked up in
+// (by its unique id) and is looked up again when the current context differs.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+template <class F>
+F driver_fn(const char *name) {
+  void *fp = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fp, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return reinterpret_cast<F>(fp);
+}
+
 constexpr int kMaxDevices = 64;
-dg::Partial *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  dg::Partial *ptr;
+};
+std::mutex g_scratch_mu;
+ScratchEntry g_scratch[kMaxDevices] = {};
 
 int scratch_for_current_device(dg::Partial **out) {
   int dev = 0;
@@ -35,64 +60,48 @@ int scratch_for_current_device(dg::Partial **out) {
     return DG_ERR_CUDA;
   }
   if (dev < 0 || dev >= kMaxDevices) return DG_ERR_UNSUPPORTED;
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return DG_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = reinterpret_cast<dg::Partial *>(p);
+  static const CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_ctx || !get_id) return DG_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return DG_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchEntry &e = g_scratch[dev];
+  if (ctx && get_id(ctx, &id) == CUDA_SUCCESS && e.ptr && e.ctx_id == id) {
+    *out = e.ptr;
+    return DG_OK;
   }
-  *out = g_scratch_ptr[dev];
+  // first call on this device, or a new context: look the address up (this
+  // also makes the device's primary context current if none was)
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return DG_ERR_CUDA;
+  }
+  if (get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return DG_ERR_CUDA;
+  e.ptr = reinterpret_cast<dg::Partial *>(p);
+  e.ctx_id = id;
+  *out = e.ptr;
   return DG_OK;
-}
-
-bool params_ok(const dg_params *p) {
-  if (!p) return false;
-  if (p->batch < 1 || p->canvas_len < 1 || p->canvas_len > 1024) return false;
-  if (p->vocab < 2) return false;
-  if (p->logits_dtype != DG_F32 && p->logits_dtype != DG_BF16) return false;
-  if (p->logits_ld < p->vocab) return false;
-  if (!(p->entropy_budget >= 0.f) || p->entropy_budget > 3.0e38f) return false;
-  if (p->conf_threshold != p->conf_threshold) return false;
-  if (p->stable_k < 1 || p->step_cap < 1) return false;
-  if (p->stop_rule != DG_STOP_ARGMAX_STABLE && p->stop_rule != DG_STOP_ENTROPY) return false;
-  if (p->accept_rule != DG_ACCEPT_ENTROPY_BUDGET && p->accept_rule != DG_ACCEPT_MONOTONE)
-    return false;
-  if (!(p->softcap >= 0.f) || p->softcap > 3.0e38f) return false;
-  if (!(p->embed_scale >= 0.f) || p->embed_scale > 3.0e38f) return false;
-  return true;
-}
-
-bool state_ok(const dg_params *p, const dg_state *st) {
-  return st && st->phase && st->request_id && st->temperature && st->rng_step && st->step &&
-         st->stable && st->canvas && st->argmax_prev && st->cand && st->argmax && st->accept &&
-         st->m && st->s && st->entropy && st->mean_entropy && st->converged && st->sc_valid &&
-         st->num_sampled && st->num_rejected && st->emitted && st->device_status &&
-         (p->accept_rule != DG_ACCEPT_MONOTONE || (st->committed && st->prev_conf));
 }
 
 }  // namespace
 
 extern "C" int dg_denoise_step_noalloc(const dg_params *p, const void *logits, const dg_state *st,
                                        cudaStream_t stream) {
-  if (!params_ok(p) || !state_ok(p, st) || !logits) return DG_ERR_INVALID_ARG;
-  const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
-  if (reinterpret_cast<uintptr_t>(logits) % esz != 0) return DG_ERR_INVALID_ARG;
+  // the same argument checks as dg_denoise_step, in the same order
+  const int rc = dg::denoise_args_ok(p, logits, st);
+  if (rc != DG_OK) return rc;
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
   const dg::VocabChunking vc = dg::vocab_chunking(n_pos, p->vocab);
   if (n_pos * (int64_t)vc.n_chunks > (int64_t)kScratchRecords) return DG_ERR_SCRATCH_LIMIT;
-  int major = 0, minor = 0, dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return DG_ERR_CUDA;
-  }
-  if (major != 10 || minor != 3) return DG_ERR_UNSUPPORTED;
+  const int dv = dg::device_ok();
+  if (dv != DG_OK) return dv;
   dg::Partial *part = nullptr;
-  const int rc = scratch_for_current_device(&part);
-  if (rc != DG_OK) return rc;
+  const int sc = scratch_for_current_device(&part);
+  if (sc != DG_OK) return sc;
   cudaGetLastError();
   if (dg::launch_vocab_pass(*p, logits, *st, part, vc.chunk, vc.n_chunks, stream) != cudaSuccess)
     return DG_ERR_CUDA;

@@ -21,6 +21,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include <cstring>
 #include <algorithm>
 
@@ -41,9 +43,21 @@ constexpr int NA = 3;    // logits / p stages of 32 KB
 constexpr int kProdWarps = 16;  // four per scheduler: the p rebuild is latency-bound
 constexpr int kAIssuers = 2;  // TMA warps that each load one 128-row half of the logits tile
 constexpr int kFirstAWarp = 2 + kProdWarps;
+#ifndef DG_K4_E_ISSUERS
+#define DG_K4_E_ISSUERS 1
+#endif
+// TMA warps for the E tile: a tiled copy holds its issuing thread for a time
+// that grows with the box's rows, so the four boxes of a stage may be split
+// between two warps (warp 0 and the last warp).
+constexpr int kEIssuers = DG_K4_E_ISSUERS;
+static_assert(kEIssuers == 1 || kEIssuers == 2, "one or two E warps");
+#ifndef DG_K4_E3D
+#define DG_K4_E3D 1
+#endif
+constexpr int kSecondEWarp = kEIssuers == 2 ? kFirstAWarp + kAIssuers : -1;
 // warp 0 E-tile TMA, warp 1 MMA, 16 producer/epilogue warps, 2 logits TMA
-// warps (20 warps: a multiple of 4, so the register cap is 96)
-constexpr int kThreads = 32 * (kFirstAWarp + kAIssuers);
+// warps, optionally a second E warp (at 96 registers a thread, 21 warps fit)
+constexpr int kThreads = 32 * (kFirstAWarp + kAIssuers + kEIssuers - 1);
 constexpr uint32_t kABytes = BM * BK * 2;  // 32 KB
 constexpr uint32_t kAHalf = 128 * BK * 2;  // 16 KB: one M=128 operand
 constexpr uint32_t kBBoxBytes = BK * 128;  // one 64-column box of E: 64 rows x 128 B
@@ -51,10 +65,10 @@ constexpr uint32_t kBBytes = BK * BN * 2;  // 32 KB
 constexpr uint32_t kSharedBytes = 1024;  // barriers + per-row flags, after the stages
 constexpr uint32_t kSmemBytes = NE * kBBytes + NA * kABytes + kSharedBytes + 1024;  // + alignment
 static_assert(kSmemBytes <= 232448, "over the 227 KB per-CTA shared memory limit");
-constexpr int kAssumedSMs = 152;
 // E tiles come mostly from DRAM, logits tiles mostly from L2 (the column tiles
-// of a row block run side by side), so one CTA per cluster asks L2 for the E
-// tile this many k-blocks before it is loaded.
+// of a row block run side by side), so the CTAs of even row tiles ask L2 for
+// the E tile this many k-blocks before it is loaded (the odd row tile next to
+// each, which runs at the same time on the same E tile, finds it there).
 constexpr int kPrefetchKb = 4;
 #ifndef DG_WAIT_NS
 #define DG_WAIT_NS 2000000000ull
@@ -63,7 +77,7 @@ constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
 
 struct Shared {
   uint64_t full[NE];     // TMA bytes of the stage's E tile landed
-  uint64_t empty[NE];    // the MMAs reading the E stage completed (every CTA of the cluster)
+  uint64_t empty[NE];    // the MMAs reading the E stage completed
   uint64_t a_full[NA];   // TMA bytes of the stage's logits tile landed
   uint64_t a_ready[NA];  // producers wrote p into the A tile
   uint64_t a_empty[NA];  // the MMAs reading the A stage completed
@@ -176,6 +190,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// One 3D box: the four 64-column blocks of a stage's E tile in one copy
+// (dimensions: column within a block, vocabulary row, block).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format); swz: 2 = 128-byte,
 // 4 = 64-byte swizzle.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
@@ -201,43 +226,6 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
 }
-// Multicast TMA load: the box lands at the same shared-memory offset in every
-// CTA of `mask`, completing bytes on each one's barrier at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                               int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-// Arrive (once) on the barrier at `bar`'s offset in every CTA of `mask` when
-// the MMAs issued so far by this thread complete.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Load a 32-bit word at `p`'s shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ int32_t ld_peer_i32(const void *p, uint32_t rank) {
-  uint32_t addr;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(addr) : "r"(smem_u32(p)), "r"(rank));
-  int32_t v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -278,8 +266,8 @@ struct GemmArgs {
   int32_t V, C, d, dtype;
   int64_t rows;  // B*C
   int32_t m_tiles, n_tiles, splits, k_blocks, kb_per_split;
-  int32_t m_groups;  // ceil(m_tiles / cluster size)
   int32_t tma_a;  // 1: bf16 logits tiles arrive by TMA; 0: producers load them
+  int32_t e3d;    // 1: tmap_e is 3D and a stage's E tile is one copy; 0: 2D, one copy per block
   const uint8_t *phase;
   const uint8_t *sc_valid;
   const float *temperature;
@@ -411,11 +399,13 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
   return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4));
 }
 
-// CL CTAs form a cluster over CL consecutive row tiles of one column tile and
-// one vocabulary split: each loads 1/CL of every E tile and multicasts it to
-// all CL, so E leaves L2 once per cluster instead of once per CTA.  CAP: the
-// producers softcap the logits before the rebuild.
-template <int CL, bool CAP>
+// One CTA per (column tile, row tile, vocabulary split), numbered with the
+// column tile fastest and the row tile next, so the CTAs that read the same
+// logits tile (all column tiles of a row tile) and those that read the same E
+// tile (all row tiles of a column tile and split) run at the same time and
+// share both through L2.  CAP: the producers softcap the logits before the
+// rebuild.
+template <bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
                          const __grid_constant__ CUtensorMap tmap_z,
@@ -428,25 +418,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared *sh = reinterpret_cast<Shared *>(smem + NE * kBBytes + NA * kABytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rank = (CL > 1) ? (int)cluster_rank() : 0;
-  const int cl = blockIdx.x / CL;
-  const int n_t = cl % a.n_tiles;
-  const int rest = cl / a.n_tiles;
-  const int m_t = (rest % a.m_groups) * CL + rank;
-  const int split = rest / a.m_groups;
-  const uint16_t cl_mask = (uint16_t)((1u << CL) - 1u);
+  const int n_t = blockIdx.x % a.n_tiles;
+  const int rest = blockIdx.x / a.n_tiles;
+  const int m_t = rest % a.m_tiles;
+  const int split = rest / a.m_tiles;
   const int64_t row0 = (int64_t)m_t * BM;
   const int n0 = n_t * BN;
   const int kb0 = split * a.kb_per_split;
   const int kb1 = min(a.k_blocks, kb0 + a.kb_per_split);
   const int nkb = max(0, kb1 - kb0);
   const int n_box = min(BN / 64, (a.d - n0 + 63) / 64);  // E boxes per stage
-  const uint32_t stage_tx = (uint32_t)n_box * kBBoxBytes;  // E bytes landing in this CTA
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NE; ++s) {
-      mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], CL);  // one MMA-commit arrival from each CTA of the cluster
+      mbar_init(&sh->full[s], kEIssuers);  // one expect-tx arrival per E warp
+      mbar_init(&sh->empty[s], 1);  // the MMA commit
     }
     for (int s = 0; s < NA; ++s) {
       mbar_init(&sh->a_full[s], kAIssuers);
@@ -474,23 +460,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL > 1) cluster_sync_all();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-  // the cluster runs its pipeline if any of its CTAs has a row to feed
-  int32_t any = 0;
-#pragma unroll
-  for (int r = 0; r < CL; ++r) any |= (CL > 1) ? ld_peer_i32(&sh->any_valid, (uint32_t)r) : sh->any_valid;
-  const bool run = any != 0 && nkb > 0;
+  // the pipeline runs if the CTA has a row to feed
+  const bool run = sh->any_valid != 0 && nkb > 0;
 
   if (run) {
-    if (warp == 0) {
+    if (warp == 0 || warp == kSecondEWarp) {
       // ------------------------------------------------ E ring (TMA)
-      // Warp 0 posts the stage's expected E bytes (all boxes, own and peers')
-      // and loads the boxes j with j % CL == rank, multicast to the cluster
-      // when CL > 1; one CTA per cluster also prefetches E into L2.
-      const bool prefetch = rank == 0;
+      // Each E warp posts the bytes of its own boxes (box j belongs to E warp
+      // j % kEIssuers) and loads them; the first also prefetches E into L2
+      // on even row tiles.
+      const int ew = warp == 0 ? 0 : 1;
+      const bool prefetch = ew == 0 && (m_t & 1) == 0;
       if (lane == 0) {
+        const int my_boxes = (n_box - ew + kEIssuers - 1) / kEIssuers;
+        // a 3D copy always fills the whole stage (blocks past d read as zeros)
+        const uint32_t my_tx = a.e3d ? (ew == 0 ? kBBytes : 0u) : (uint32_t)my_boxes * kBBoxBytes;
         if (prefetch)
           for (int i = 0; i < min(kPrefetchKb, nkb); ++i)
             tma_prefetch_2d(&tmap_ep, n0, (kb0 + i) * BK);
@@ -502,14 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
             break;
           const int32_t kv = (kb0 + i) * BK;
-          mbar_expect_tx(&sh->full[s], stage_tx);
+          mbar_expect_tx(&sh->full[s], my_tx);
           uint8_t *dstB = sB + s * kBBytes;
-          for (int j = rank; j < n_box; j += CL) {
-            if (CL == 1)
+          if (a.e3d) {
+            if (ew == 0) tma_load_3d(dstB, &tmap_e, &sh->full[s], 0, kv, n0 / 64);
+          } else {
+            for (int j = ew; j < n_box; j += kEIssuers)
               tma_load_2d(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv);
-            else
-              tma_load_2d_mc(dstB + j * kBBoxBytes, &tmap_e, &sh->full[s], n0 + j * 64, kv,
-                             cl_mask);
           }
           if (prefetch && i + kPrefetchKb < nkb)
             tma_prefetch_2d(&tmap_ep, n0, (kb0 + i + kPrefetchKb) * BK);
@@ -562,11 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_bf16(tmem + (uint32_t)(mh * BN), ad, bd, (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          if (CL == 1)
-            mma_commit(&sh->empty[s]);
-          else
-            mma_commit_mc(&sh->empty[s], cl_mask);  // every CTA may now reuse E stage s
-          mma_commit(&sh->a_empty[sa]);             // this CTA may reuse A stage sa
+          mma_commit(&sh->empty[s]);    // the E warps may reuse E stage s
+          mma_commit(&sh->a_empty[sa]);  // the logits warps may reuse A stage sa
         }
         mma_commit(&sh->tmem_full);
         mma_commit(&sh->mma_done);
@@ -750,9 +732,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * BN));
   }
-  // no CTA leaves while a peer may still signal its barriers or write its
-  // shared memory
-  if (CL > 1) cluster_sync_all();
 }
 
 // out[q, :] = sum over splits of the partial sums, zeros for rows that do
@@ -813,27 +792,22 @@ cudaError_t dg_selfcond_wait_record(uint32_t out[4]) {
   return cudaMemcpyFromSymbol(out, g_wait_record, sizeof(uint32_t) * 4);
 }
 
-SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms) {
   SelfcondPlan pl;
   pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
   pl.n_tiles = (d + BN - 1) / BN;
   pl.k_blocks = (V + BK - 1) / BK;
-  // clusters of 2 row tiles share every E tile (multicast); a lone row tile
-  // runs alone
-  pl.cluster = pl.m_tiles >= 2 ? 2 : 1;
-  pl.m_groups = (pl.m_tiles + pl.cluster - 1) / pl.cluster;
-  const int64_t m_pad = (int64_t)pl.m_groups * pl.cluster;
-  const int64_t tiles = m_pad * pl.n_tiles;
-  // Choose the split count whose CTA count fills the SMs best (waves of
-  // kAssumedSMs), keeping at least 16 k-blocks per split.
+  const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
+  const int64_t sms = n_sms > 0 ? n_sms : 1;
+  // Choose the split count whose CTA count fills the SMs best (waves of one
+  // CTA per SM), keeping at least 16 k-blocks per split.
   int best = 1;
   double best_eff = 0.0;
   for (int sp = 1; sp <= 64; ++sp) {
     if (sp > 1 && pl.k_blocks / sp < 16) break;
     const int64_t ctas = tiles * sp;
-    const int64_t waves = (ctas + kAssumedSMs - 1) / kAssumedSMs;
-    const double work = (double)pl.m_tiles * (double)pl.n_tiles * sp;
-    const double eff = work / (double)(waves * kAssumedSMs);
+    const int64_t waves = (ctas + sms - 1) / sms;
+    const double eff = (double)ctas / (double)(waves * sms);
     if (eff > best_eff + 0.05) {
       best_eff = eff;
       best = sp;
@@ -842,39 +816,28 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d) {
   const int32_t kbps = (pl.k_blocks + best - 1) / best;
   pl.kb_per_split = kbps;
   pl.splits = (pl.k_blocks + kbps - 1) / kbps;
+  pl.n_sms = (int32_t)sms;
   pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0;
   return pl;
 }
 
 namespace {
-template <int CL, bool CAP>
+template <bool CAP>
 cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
                         const CUtensorMap &map_ep, const GemmArgs &a, int64_t grid,
                         cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {false};
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CL, CAP>,
+  static std::atomic<bool> attr_set[64];  // the shared-memory limit is raised once per device
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CAP>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  cudaLaunchConfig_t cfg;
-  memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, selfcond_gemm_kernel<CL, CAP>, map_e, map_z, map_ep, a);
+  selfcond_gemm_kernel<CAP><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map_e, map_z, map_ep, a);
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -886,7 +849,24 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   if (!enc) return cudaErrorNotSupported;
   const int64_t rows = (int64_t)p.batch * p.canvas_len;
   CUtensorMap map_e, map_z, map_ep;
-  {
+  // With d a multiple of 64, E is also a 3D tensor (column within a 64-column
+  // block, vocabulary row, block), and a stage's four blocks are one copy:
+  // a copy holds its issuing thread for a time that grows with its rows, and
+  // one 3D copy of 4 x 64 rows holds it for less than four 2D copies of 64.
+  // Every element of the 3D view lies inside E (blocks past d are outside
+  // the tensor and read as zeros).
+  bool e3d = DG_K4_E3D && d % 64 == 0;
+  if (e3d) {
+    const cuuint64_t dims[3] = {64, (cuuint64_t)p.vocab, (cuuint64_t)(d / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld_E * 2, 128};
+    const cuuint32_t box[3] = {64, (cuuint32_t)BK, (cuuint32_t)(BN / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    e3d = enc(&map_e, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(E), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  if (!e3d) {
     const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)p.vocab};
     const cuuint64_t strides[1] = {(cuuint64_t)ld_E * 2};
     const cuuint32_t box[2] = {64, (cuuint32_t)BK};
@@ -931,12 +911,12 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.dtype = p.logits_dtype;
   a.rows = rows;
   a.m_tiles = plan.m_tiles;
-  a.m_groups = plan.m_groups;
   a.n_tiles = plan.n_tiles;
   a.splits = plan.splits;
   a.k_blocks = plan.k_blocks;
   a.kb_per_split = plan.kb_per_split;
   a.tma_a = tma_a ? 1 : 0;
+  a.e3d = e3d ? 1 : 0;
   a.phase = st.phase;
   a.sc_valid = st.sc_valid;
   a.temperature = st.temperature;
@@ -951,20 +931,16 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.cap_c = cap ? p.softcap : 0.f;
   a.scale = p.embed_scale > 0.f ? p.embed_scale : 1.0f;
 
-  const int64_t grid = (int64_t)plan.m_groups * plan.cluster * plan.n_tiles * plan.splits;
-  cudaError_t e;
-  if (plan.cluster == 2)
-    e = cap ? launch_gemm<2, true>(map_e, map_z, map_ep, a, grid, s)
-            : launch_gemm<2, false>(map_e, map_z, map_ep, a, grid, s);
-  else
-    e = cap ? launch_gemm<1, true>(map_e, map_z, map_ep, a, grid, s)
-            : launch_gemm<1, false>(map_e, map_z, map_ep, a, grid, s);
+  const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
+  cudaError_t e = cap ? launch_gemm<true>(map_e, map_z, map_ep, a, grid, s)
+                      : launch_gemm<false>(map_e, map_z, map_ep, a, grid, s);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (plan.splits > 1) {
+    // a grid-stride loop over float4 columns: 16 CTAs of 256 threads per SM
     const int64_t n4 = a.rows * (d / 4);
-    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, 152 * 16);
+    const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, (int64_t)plan.n_sms * 16);
     selfcond_reduce_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
     e = cudaGetLastError();
   }

@@ -15,6 +15,8 @@
 // +inf or -inf logit are redone on a careful scalar path.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "dg_device.cuh"
 #include "dg_internal.h"
 
@@ -792,15 +794,15 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   {
-    static bool attr_set[64] = {false};
+    static std::atomic<bool> attr_set[64];  // the shared-memory limit is raised once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
       e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) attr_set[dev] = true;
+      if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
     }
   }
   const bool cap = p.softcap > 0.f;

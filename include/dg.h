@@ -148,7 +148,9 @@ typedef struct {
 /* Bytes of caller workspace needed by dg_denoise_step and, if d > 0, by
  * dg_selfcond_embed with embedding width d (one buffer serves both, as the
  * calls are ordered on one stream).  Returns 0 if `p` is invalid.  Depends on
- * the sizes in `p` and on d only. */
+ * the sizes in `p`, on d and on the SM count of the current device (the
+ * self-conditioning GEMM splits the vocabulary to fill the SMs in whole
+ * waves); query it with the device current that the calls will run on. */
 size_t dg_workspace_bytes(const dg_params *p, int32_t d);
 
 /* Stand-alone canvas initialisation (the prefill case) of the rows r with
@@ -226,13 +228,15 @@ int dg_anneal_temperature(const dg_params *p, const int32_t *step, float *temper
  * dg_denoise_step; the scratch it needs (one 32-byte record per position and
  * vocabulary chunk) lives in a 2 MiB array inside the library that every GPU
  * loading the library keeps until the process exits.  Limit: batch *
- * canvas_len * chunks <= 65536 records (for example 32768 positions at
- * V = 262144, or 2048 positions of 8 chunks each); larger problems return
- * DG_ERR_SCRATCH_LIMIT before anything is enqueued.  The first call on a
- * device looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Calls
- * share the array, so two calls whose kernels may overlap on the GPU race:
- * order them on one stream.  Allocates and frees nothing. */
+ * canvas_len * chunks <= 65536 records (V = 262144 takes 8 chunks per
+ * position up to 1216 positions, 4 up to 9728 and 2 beyond, so up to 32768
+ * positions fit); larger problems return DG_ERR_SCRATCH_LIMIT before
+ * anything is enqueued.  The first call on a device, and the first call in a
+ * new context of that device (after cudaDeviceReset), looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  Calls share the array, so two calls
+ * whose kernels may overlap on the GPU race: order them on one stream.
+ * Allocates and frees nothing. */
 int dg_denoise_step_noalloc(const dg_params *p, const void *logits, const dg_state *st,
                             cudaStream_t stream);
 
