@@ -107,7 +107,7 @@ class Flags:
 
     cand: np.ndarray = None      # bool [B, C]: top-2 perturbed-score gap < 1e-4
     accept: np.ndarray = None    # bool [B]: acceptance cut within 1e-4
-    converged: np.ndarray = None  # bool [B]: |mean H - thr| < 1e-4
+    converged: np.ndarray = None  # bool [B]: |mean H - thr| < 1e-4 where thr decides
     gaps: np.ndarray = None      # float64 [B, C]
     commit: np.ndarray = None    # bool [B, C]: |conf - prev_conf| < 1e-4 (monotone rule)
 
@@ -353,7 +353,17 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=m
         conv = st.stable[r] >= p.stable_k or st.step[r] >= p.step_cap
     else:
         conv = (st.stable[r] >= p.stable_k and Hbar < p.conf_threshold) or st.step[r] >= p.step_cap
-    flags.converged[r] = (not math.isnan(Hbar)) and abs(Hbar - p.conf_threshold) < NEAR_TIE
+    # Near-tie flag of the convergence decision (a reading of the near-tie
+    # rule for the mean-entropy threshold): the mean entropy lies within 1e-4
+    # of the threshold AND the threshold decides something.  Under the
+    # entropy-only stop it decides the stable counter itself; under the
+    # argmax-stable rule only a row whose argmax has been stable for stable_k
+    # steps and that is below the step cap depends on it.
+    near = (not math.isnan(Hbar)) and abs(Hbar - p.conf_threshold) < NEAR_TIE
+    if p.stop_rule == STOP_ENTROPY:
+        flags.converged[r] = near
+    else:
+        flags.converged[r] = near and st.stable[r] >= p.stable_k and st.step[r] < p.step_cap
     st.converged[r] = 1 if conv else 0
     st.sc_valid[r] = 0 if conv else 1
     st.phase[r] = PHASE_COMMIT if conv else PHASE_DENOISE

@@ -92,13 +92,43 @@ def run_oracle_step(p: dg.Params, snap_before: dict, logits_host, rows=None):
     return osam.step(op, st0, _Rows(), rows=rows, mapper=pmap)
 
 
+def flag_bounds(n_rows: int, n_positions: int):
+    """Most near-tie flags one compared step may carry: near ties are rare
+    (a top-2 gap or an entropy distance below 1e-4), so a step whose flags
+    exceed these bounds points at a fault, not at chance.  Rows: 1, or 2 %
+    of the compared rows; positions: 2, or 1 % of them."""
+    return max(1, -(-2 * n_rows // 100)), max(2, n_positions // 100)
+
+
+def _cut_prefix_error(H_gpu, H_ref, acc_ref):
+    """|GPU prefix - oracle prefix| of the sorted entropies: the largest over
+    all exclusive prefixes and the one at the acceptance cut.  Both prefixes
+    follow the oracle's (H, i) order; the GPU's prefix is the exact sum of
+    its fp32 entropies, as its canvas kernel forms it."""
+    valid = ~np.isnan(H_ref)
+    order = sorted(np.flatnonzero(valid), key=lambda i: (H_ref[i], i))
+    if not order:
+        return 0.0, 0.0
+    g = np.cumsum(np.concatenate([[0.0], np.asarray(H_gpu, np.float64)[order][:-1]]))
+    o = np.cumsum(np.concatenate([[0.0], np.asarray(H_ref, np.float64)[order][:-1]]))
+    d = np.abs(g - o)
+    n_acc = int(np.asarray(acc_ref).sum())
+    k = min(max(n_acc, 1), len(order) - 1) if len(order) > 1 else 0
+    return float(d.max()), float(d[k])
+
+
 def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags: osam.Flags,
-                 rows=None, positions=None):
+                 rows=None, positions=None, bound_flags: bool = True):
     """Assert the GPU's post-step state equals the oracle's, up to tolerances
-    and the oracle's near-tie flags.  Returns counts of flagged decisions."""
+    and the oracle's near-tie flags, and (bound_flags) that the flagged
+    decisions stay within flag_bounds.  Returns counts of flagged decisions
+    and, under the budget rule, the largest prefix error of the sorted
+    entropies (all prefixes; and at the acceptance cut), which must stay
+    below the 1e-4 window of the acceptance flag."""
     B, C = p.batch, p.canvas_len
     rows = range(B) if rows is None else rows
-    n_flag = {"cand": 0, "accept": 0, "converged": 0}
+    n_flag = {"cand": 0, "accept": 0, "converged": 0, "prefix_err": 0.0, "cut_err": 0.0}
+    n_denoise = 0
     for r in rows:
         ph = int(before["phase"][r])
         sl = slice(r * C, (r + 1) * C)
@@ -119,6 +149,7 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
                 assert np.all(g["committed"][sl] == 0) and np.all(np.isinf(g["prev_conf"][sl])), r
             continue
         # DENOISE
+        n_denoise += 1
         valid = ~np.isnan(ost.entropy[r])
         assert np.array_equal(np.isnan(g["entropy"][sl]), ~valid), (r, "validity")
         v = valid
@@ -143,6 +174,13 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
             assert np.array_equal(g["canvas"][sl][ok], ost.canvas[r][ok]), (r, "canvas")
             rel = np.abs(g["prev_conf"][sl][v] / ost.prev_conf[r][v] - 1.0)
             assert np.all(rel <= S_RTOL), (r, "prev_conf", float(rel.max()))
+        else:
+            pe, ce = _cut_prefix_error(g["entropy"][sl], ost.entropy[r], ost.accept[r])
+            n_flag["prefix_err"] = max(n_flag["prefix_err"], pe)
+            n_flag["cut_err"] = max(n_flag["cut_err"], ce)
+            assert ce < osam.NEAR_TIE, (r, "prefix error at the cut", ce)
+        if p.accept_rule == dg.DG_ACCEPT_MONOTONE:
+            pass  # compared above, position by position
         elif flags.accept[r]:
             n_flag["accept"] += 1
         else:
@@ -154,13 +192,25 @@ def compare_step(p: dg.Params, before: dict, after: dict, ost: osam.State, flags
             assert np.isnan(g["mean_entropy"][r])
         else:
             assert abs(g["mean_entropy"][r] - mh) <= ENT_TOL, (r, "mean_entropy")
-        for k in ("step", "stable", "num_sampled", "num_rejected"):
+        for k in ("step", "num_sampled", "num_rejected"):
             assert g[k][r] == getattr(ost, k)[r], (r, k)
         if flags.converged[r]:
             n_flag["converged"] += 1
+            # under the entropy-only stop the threshold also decides the
+            # stable counter; under the argmax-stable rule it does not
+            if p.stop_rule != dg.DG_STOP_ENTROPY:
+                assert g["stable"][r] == ost.stable[r], (r, "stable")
         else:
-            for k in ("converged", "sc_valid", "phase"):
+            for k in ("stable", "converged", "sc_valid", "phase"):
                 assert g[k][r] == getattr(ost, k)[r], (r, k)
+    if bound_flags:
+        max_rows, max_pos = flag_bounds(n_denoise, n_denoise * C)
+        assert n_flag["cand"] <= max_pos, n_flag
+        if p.accept_rule == dg.DG_ACCEPT_MONOTONE:
+            assert n_flag["accept"] <= max_pos, n_flag
+        else:
+            assert n_flag["accept"] <= max_rows, n_flag
+        assert n_flag["converged"] <= max_rows, n_flag
     return n_flag
 
 
