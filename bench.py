@@ -4,15 +4,22 @@ vocabulary pass + per-canvas acceptance / re-noise / convergence) followed by
 dg_selfcond_embed (the tcgen05 softmax(z/T).E contraction), over one batch of
 synthetic logits resident in HBM.
 
-Default workload: 8 canvases x 256 positions (2048 positions), V = 262144,
-bf16 logits N(0, 2^2) plus U[0,16) on one token per position, T = 0.8,
-budget 96 nats, E 262144 x 2816 bf16 ~ N(0, 0.02^2).  The step cap is lifted
-so that every timed step does the full work (all rows stay in DENOISE and
-feed the self-conditioning).  Inputs (1.07 GB logits, 1.48 GB E) are larger
-than L2, so no flush is needed between steps.
+Default workload: the largest single-GPU batch, 128 canvases x 256 positions
+(32768 positions), V = 262144, bf16 logits N(0, 2^2) plus U[0,16) on one
+token per position (17.2 GB), T = 0.8, budget 128 nats, E 262144 x 2816 bf16
+~ N(0, 0.02^2).  The step cap is lifted so that every timed step does the
+full work (all rows stay in DENOISE and feed the self-conditioning).  Inputs
+are larger than L2, so no flush is needed between steps.  The default 60
+timed steps take about 2.4 s, long enough for the power-capped steady state.
+
+Other modes: ``--workload`` picks another batch (8 canvases, the sweep, one
+canvas); ``--mode mixed-loop`` runs the 32-request mixed-phase loop (8
+prefill, 20 denoise, 4 commit) until every request has committed;
+``--mode graph-loop`` times the one-canvas 24-step loop eagerly and as a
+CUDA-graph replay.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle
-on the same workload instead (a bounded sample per step).
+on the same workload instead (a bounded sample per step, one thread).
 """
 
 from __future__ import annotations
@@ -41,7 +48,7 @@ WORKLOADS = {
     "128x256-V262144-bf16-d2816": (128, 256, 262144, "bf16", 0.8, 128.0, 2816, 16.0),
     "1x256-V262144-bf16-d2816": (1, 256, 262144, "bf16", 0.8, 96.0, 2816, 16.0),
 }
-DEFAULT = "8x256-V262144-bf16-d2816"
+DEFAULT = "128x256-V262144-bf16-d2816"
 METRIC = "denoise-step positions/s (sampler+self-cond)"
 SEED = 0xD1FF0002
 
@@ -304,11 +311,12 @@ def run_ours(args, rank, world, dev):
         # its logits from pinned host memory and reads its outputs back.  Two
         # device buffers let the copy of step k+1 run on a copy stream while
         # step k computes, as a serving loop would overlap them.
-        host_logits = [torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
-                       for _ in range(2)]
-        for hb in host_logits:
-            hb.copy_(logits)
-        dev_logits = [torch.empty_like(logits) for _ in range(2)]
+        # one pinned host copy of the logits serves every step (17 GB at the
+        # default workload); two device buffers alternate
+        host = torch.empty(logits.shape, dtype=logits.dtype, pin_memory=True)
+        host.copy_(logits)
+        host_logits = [host, host]
+        dev_logits = [logits, torch.empty_like(logits)]
         host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         host_canvas = torch.empty(st.canvas.shape, dtype=st.canvas.dtype, pin_memory=True)
         copy_stream = torch.cuda.Stream(dev)
@@ -338,7 +346,7 @@ def run_ours(args, rank, world, dev):
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
-        Ke = max(2, K // 4)
+        Ke = max(2, min(K // 4, 8))
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -496,6 +504,91 @@ def run_graph_loop(args, dev):
             "device_status": int(st.device_status.item())}
 
 
+def run_mixed_loop(args, dev):
+    """The mixed-phase loop: 32 request slots, 8 in prefill, 20 in denoise and
+    4 in commit (their argmax canvas pre-seeded with the generator's clean
+    argmax), V = 262144, d = 2816, per-request temperatures U[0.6, 1.2],
+    stable_k = 3, threshold 0.3 nats, step cap 32, budget 96 nats.  Logits at
+    loop step s come from (seed, request, s) with the true tokens boosted by
+    2 + 0.5 s, so confidence rises and requests converge or reach the cap.
+    The loop runs until every request has committed once.  Each step's logits
+    are generated before its timed region (CUDA events around the library
+    calls); positions/s counts the denoise positions the steps processed."""
+    import torch
+    import denoise_step_sampler_gb300 as dg
+    from denoise_step_sampler_gb300 import build as dgbuild
+    from denoise_step_sampler_gb300 import synthetic as syn
+
+    dgbuild.build()
+    B, C, V, d = 32, 256, 262144, 2816
+    seed = 0xD1FF0003
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=seed,
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=32)
+    temps = syn.temperatures(B, seed=seed, device="cpu")
+    phases = torch.tensor([dg.DG_PHASE_PREFILL] * 8 + [dg.DG_PHASE_DENOISE] * 20 +
+                          [dg.DG_PHASE_COMMIT] * 4, dtype=torch.uint8)
+    prev = torch.zeros((B, C), dtype=torch.int32)
+    for r in range(28, 32):
+        prev[r] = syn.true_tokens(C, V, seed=seed, request=r).to(torch.int32)
+    E = syn.embedding(V, d, seed=seed + 1, device=dev)
+    ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device=dev)
+    out = torch.empty((B * C, d), dtype=torch.float32, device=dev)
+    logits = torch.empty((B, C, V), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fresh():
+        st = dg.State(B, C, dev)
+        st.phase.copy_(phases)
+        st.request_id.copy_(torch.arange(B))
+        st.temperature.copy_(temps)
+        st.argmax_prev.copy_(prev.reshape(-1))
+        return st
+
+    def loop(st, max_steps, timed):
+        committed = torch.zeros(B, dtype=torch.bool)
+        ev, den_pos = [], 0
+        for s_ in range(max_steps):
+            ph = st.phase.cpu()
+            committed |= ph == dg.DG_PHASE_COMMIT
+            if committed.all():
+                break
+            for r in range(B):
+                if ph[r] == dg.DG_PHASE_DENOISE:
+                    syn.loop_logits(C, V, seed=seed, request=r, step=s_, out=logits[r],
+                                    device=dev)
+            den_pos += int((ph == dg.DG_PHASE_DENOISE).sum()) * C
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            e[0].record(stream)
+            dg.dg_denoise_step(p, logits.view(-1), st, ws)
+            dg.dg_selfcond_embed(p, logits.view(-1), st, E, out, ws)
+            e[1].record(stream)
+            ev.append(e)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev], den_pos, bool(committed.all())
+
+    loop(fresh(), args.warmup, False)
+    st = fresh()
+    clocks = ClockSampler(gpu_id_for(dev))
+    clocks.start()
+    time.sleep(0.3)
+    ms, den_pos, done = loop(st, 40, True)
+    clk = clocks.stop()
+    total = sum(ms)
+    return {"metric": "mixed-phase loop denoise positions/s (sampler+self-cond)",
+            "value": den_pos / (total / 1e3), "unit": "positions/s", "higher_is_better": True,
+            "n_gpus": 1, "steps": len(ms), "warmup": args.warmup,
+            "ms_per_step": total / len(ms), "ms_per_step_min": min(ms),
+            "ms_per_step_max": max(ms), "denoise_positions": den_pos,
+            "every_request_committed": done, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "mixed-32 loop (8 prefill / 20 denoise / 4 commit) "
+                                   "V262144-bf16-d2816", "cap": 32, "stable_k": 3,
+                       "conf_threshold": 0.3, "entropy_budget": 96.0,
+                       "temperature": "U[0.6, 1.2] per request",
+                       "l2": "inputs larger than L2 (up to 2.68 GB of denoise logits a step)"},
+            "clocks": clk, "gpu_launches": len(ms) * (2 + _selfcond_launches(p, d)),
+            "device_status": int(st.device_status.item())}
+
+
 # ---------------------------------------------------------- reference arm
 
 def run_reference(args, rank, world):
@@ -546,17 +639,16 @@ def run_reference(args, rank, world):
 
 
 def _threads_used() -> int:
-    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        v = os.environ.get(k)
-        if v and v.isdigit():
-            return int(v)
-    return os.cpu_count() or 1
+    """Threads the oracle arm ran on: its per-position loop is plain Python
+    and numpy on one thread, and main() runs it with one BLAS thread."""
+    v = os.environ.get("OPENBLAS_NUM_THREADS")
+    return int(v) if v and v.isdigit() else 1
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
@@ -569,8 +661,9 @@ def main():
                     help="argmax-stable convergence or the entropy-only stop")
     ap.add_argument("--anneal", action="store_true",
                     help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
-    ap.add_argument("--mode", default="step", choices=["step", "graph-loop"],
-                    help="step: the throughput line (default); graph-loop: one-canvas loop latency")
+    ap.add_argument("--mode", default="step", choices=["step", "graph-loop", "mixed-loop"],
+                    help="step: the throughput line (default); graph-loop: one-canvas loop "
+                         "latency; mixed-loop: the 32-request mixed-phase loop")
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="logit softcap c (c tanh(z / c) before the pass); 0 = off")
     ap.add_argument("--embed-scale", type=float, default=0.0,
@@ -592,7 +685,18 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.gpus != world:
+        ap.error(f"--gpus {args.gpus} but {world} process(es): launch N > 1 GPUs with "
+                 "torch.distributed.run --nproc-per-node N")
     if args.impl == "reference":
+        if os.environ.get("DG_REFERENCE_CHILD") != "1":
+            # the oracle runs single-threaded: its BLAS calls get one thread,
+            # set before numpy loads in a child process
+            env = dict(os.environ, DG_REFERENCE_CHILD="1", OMP_NUM_THREADS="1",
+                       OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+            r = subprocess.run([sys.executable, os.path.abspath(__file__)] + sys.argv[1:],
+                               env=env)
+            sys.exit(r.returncode)
         line = run_reference(args, rank, world)
         if line is not None:
             print(json.dumps(line))
@@ -606,6 +710,8 @@ def main():
     dev = torch.device("cuda", local)
     if args.mode == "graph-loop":
         line = run_graph_loop(args, dev) if rank == 0 else None
+    elif args.mode == "mixed-loop":
+        line = run_mixed_loop(args, dev) if rank == 0 else None
     else:
         line = run_ours(args, rank, world, dev)
     if line is not None:

@@ -23,7 +23,7 @@ __all__ = [
     "Params", "State", "DgError", "lib", "library_path",
     "dg_workspace_bytes", "dg_init_canvas", "dg_denoise_step", "dg_selfcond_embed",
     "dg_commit", "dg_status_string", "dg_debug_wait_record", "dg_denoise_step_noalloc",
-    "DG_ERR_SCRATCH_LIMIT",
+    "DG_ERR_SCRATCH_LIMIT", "load",
 ]
 
 DG_OK, DG_ERR_INVALID_ARG, DG_ERR_UNSUPPORTED, DG_ERR_WORKSPACE, DG_ERR_CUDA = 0, 1, 2, 3, 4
@@ -75,31 +75,36 @@ class DgError(RuntimeError):
 _LIB = None
 
 
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of the library at ``path`` with the C signatures declared
+    (``lib()`` loads the default build; tests load the wait test build)."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run `python -m denoise_step_sampler_gb300.build`")
+    L = ctypes.CDLL(path)
+    P, S = ctypes.POINTER(_CParams), ctypes.POINTER(_CState)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    L.dg_workspace_bytes.argtypes, L.dg_workspace_bytes.restype = [P, i32], sz
+    L.dg_init_canvas.argtypes, L.dg_init_canvas.restype = [P, S, vp, vp], ctypes.c_int
+    L.dg_commit.argtypes, L.dg_commit.restype = [P, S, vp, vp], ctypes.c_int
+    L.dg_denoise_step.argtypes = [P, vp, S, vp, sz, vp]
+    L.dg_denoise_step.restype = ctypes.c_int
+    L.dg_selfcond_embed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
+    L.dg_selfcond_embed.restype = ctypes.c_int
+    L.dg_status_string.argtypes, L.dg_status_string.restype = [ctypes.c_int], ctypes.c_char_p
+    L.dg_denoise_step_noalloc.argtypes = [P, vp, S, vp]
+    L.dg_denoise_step_noalloc.restype = ctypes.c_int
+    L.dg_debug_wait_record.argtypes = [vp]
+    L.dg_debug_wait_record.restype = ctypes.c_int
+    L.dg_anneal_temperature.argtypes = [P, vp, vp, ctypes.c_float, ctypes.c_float, i32, vp, vp]
+    L.dg_anneal_temperature.restype = ctypes.c_int
+    return L
+
+
 def lib():
     """Load ``libdg.so`` (built in-tree by ``denoise_step_sampler_gb300.build``)."""
     global _LIB
     if _LIB is None:
-        path = library_path()
-        if not os.path.exists(path):
-            raise RuntimeError(f"{path} is not built; run `python -m denoise_step_sampler_gb300.build`")
-        L = ctypes.CDLL(path)
-        P, S = ctypes.POINTER(_CParams), ctypes.POINTER(_CState)
-        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
-        L.dg_workspace_bytes.argtypes, L.dg_workspace_bytes.restype = [P, i32], sz
-        L.dg_init_canvas.argtypes, L.dg_init_canvas.restype = [P, S, vp, vp], ctypes.c_int
-        L.dg_commit.argtypes, L.dg_commit.restype = [P, S, vp, vp], ctypes.c_int
-        L.dg_denoise_step.argtypes = [P, vp, S, vp, sz, vp]
-        L.dg_denoise_step.restype = ctypes.c_int
-        L.dg_selfcond_embed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
-        L.dg_selfcond_embed.restype = ctypes.c_int
-        L.dg_status_string.argtypes, L.dg_status_string.restype = [ctypes.c_int], ctypes.c_char_p
-        L.dg_denoise_step_noalloc.argtypes = [P, vp, S, vp]
-        L.dg_denoise_step_noalloc.restype = ctypes.c_int
-        L.dg_debug_wait_record.argtypes = [vp]
-        L.dg_debug_wait_record.restype = ctypes.c_int
-        L.dg_anneal_temperature.argtypes = [P, vp, vp, ctypes.c_float, ctypes.c_float, i32, vp, vp]
-        L.dg_anneal_temperature.restype = ctypes.c_int
-        _LIB = L
+        _LIB = load(library_path())
     return _LIB
 
 

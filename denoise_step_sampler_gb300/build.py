@@ -33,9 +33,10 @@ def nvcc() -> str:
     return path
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc(), *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, defines=()) -> str:
+    tag = "_waittest" if defines else ""
+    obj = os.path.join(BUILD, os.path.splitext(src)[0] + tag + ".o")
+    cmd = [nvcc(), *ARCH, *FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -47,25 +48,41 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
 
 
 def _stale() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not os.path.exists(WAIT_TEST_LIB):
         return True
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(WAIT_TEST_LIB))
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "dg.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not _stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+# A test build of the library (same sources) whose self-conditioning GEMM has
+# a 1 ms bound on its pipeline waits and withholds the E copies of its third
+# k-block, so that the MMA issuer's wait for them runs out: the bounded-wait
+# exit path, tested without any fault.  Only the GEMM's object differs.
+WAIT_TEST_LIB = os.path.join(HERE, "libdg_waittest.so")
+WAIT_TEST_DEFINES = ["-DDG_WAIT_NS=1000000ull", "-DDG_TEST_WITHHOLD_E_STAGE=2"]
+
+
+def _link(objs, out):
+    tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, out)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+    """libdg.so and the wait test build libdg_waittest.so, if stale."""
+    if not force and not _stale():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    jobs = [(s, []) for s in SOURCES] + [("dg_selfcond.cu", WAIT_TEST_DEFINES)]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], verbose_ptxas, j[1]), jobs))
+    _link(objs[:len(SOURCES)], LIB)
+    test_objs = [o for src, o in zip(SOURCES, objs) if src != "dg_selfcond.cu"] + [objs[-1]]
+    _link(test_objs, WAIT_TEST_LIB)
     return LIB
 
 

@@ -73,7 +73,14 @@ constexpr int kPrefetchKb = 4;
 #ifndef DG_WAIT_NS
 #define DG_WAIT_NS 2000000000ull
 #endif
-constexpr unsigned long long kWaitNs = DG_WAIT_NS;  // bound on any single wait
+// Bound on any single pipeline wait.  Waits for copies or MMAs already issued
+// (before a CTA exits or frees its TMEM) always keep the 2 s bound: those
+// complete on their own, so the CTA never leaves with work in flight.
+constexpr unsigned long long kWaitNs = DG_WAIT_NS;
+constexpr unsigned long long kDrainNs = 2000000000ull;
+// DG_TEST_WITHHOLD_E_STAGE (test builds only): the E warps stop before
+// issuing that k-block's copies, so the MMA issuer's wait for it can only run
+// out, which exercises the bounded-wait exit path without faulting anything.
 
 struct Shared {
   uint64_t full[NE];     // TMA bytes of the stage's E tile landed
@@ -171,7 +178,7 @@ __device__ __noinline__ void mbar_drain(uint64_t *b, uint32_t parity) {
     if ((it & 255u) != 0u) continue;
     const uint64_t now = globaltimer();
     if (t0 == 0) t0 = now;
-    else if (now - t0 > kWaitNs) return;
+    else if (now - t0 > kDrainNs) return;
   }
 }
 
@@ -487,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i >= NE &&
               !mbar_wait(&sh->empty[s], (use - 1) & 1u, sh, a.status, where_code(0, 2, s, i)))
             break;
+#ifdef DG_TEST_WITHHOLD_E_STAGE
+          if (i == DG_TEST_WITHHOLD_E_STAGE) break;
+#endif
           const int32_t kv = (kb0 + i) * BK;
           mbar_expect_tx(&sh->full[s], my_tx);
           uint8_t *dstB = sB + s * kBBytes;

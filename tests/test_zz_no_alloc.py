@@ -48,12 +48,20 @@ def _compare(a, b):
         f = ~np.isnan(a[k])
         assert np.all(np.abs(a[k][f] - b[k][f]) <= ENT_TOL), k
     assert np.allclose(a["s"], b["s"], rtol=1e-5, atol=0.0, equal_nan=True)
+    # the unchanged-or-stronger rule's per-position state
+    assert np.array_equal(a["committed"], b["committed"])
+    assert np.allclose(a["prev_conf"], b["prev_conf"], rtol=1e-5, atol=0.0, equal_nan=True)
 
 
-@pytest.mark.parametrize("B,C,V,dt", [(3, 256, 50257, dg.DG_BF16), (2, 64, 3001, dg.DG_F32)])
-def test_noalloc_step_matches_workspace_step_twice(B, C, V, dt):
+@pytest.mark.parametrize("B,C,V,dt,rule", [
+    (3, 256, 50257, dg.DG_BF16, dg.DG_ACCEPT_ENTROPY_BUDGET),
+    (2, 64, 3001, dg.DG_F32, dg.DG_ACCEPT_ENTROPY_BUDGET),
+    (3, 128, 4099, dg.DG_BF16, dg.DG_ACCEPT_MONOTONE),
+])
+def test_noalloc_step_matches_workspace_step_twice(B, C, V, dt, rule):
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dt, seed=77,
-                  entropy_budget=40.0, conf_threshold=0.3, stable_k=1, step_cap=8)
+                  entropy_budget=40.0, conf_threshold=0.3, stable_k=1, step_cap=8,
+                  accept_rule=rule)
     temps = list(np.linspace(0.7, 1.2, B))
     tdt = torch.bfloat16 if dt == dg.DG_BF16 else torch.float32
     ref, new = _state(p, temps), _state(p, temps)
