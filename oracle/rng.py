@@ -28,6 +28,13 @@ and every other member is the minimum plus a fresh Exp(1).  Groups are the
     X_g = exp1(draw32(K_GMIN, g)),   J_g = below(draw32(K_GARG, g), n_g),
     E_v = X_g / n_g + [v - 8g != J_g] * exp1(draw32(K_GREST, v)),
     G_v = -ln E_v  (standard Gumbel).
+
+The segmented (hierarchical) Gumbel-max rule uses tags SEG and WITHIN over a
+fixed partition of the vocabulary into segments of 32 indices: superblock j
+holds the indices [1024 j, 1024 j + 1024), and its segment l (0 <= l < 32)
+the four groups of 8 at offsets 8 l, 256 + 8 l, 512 + 8 l and 768 + 8 l, so
+segment k = 32 j + l holds {1024 j + 256 u + 8 l + t : 0 <= u < 4,
+0 <= t < 8} (indices >= V left out).
 """
 
 from __future__ import annotations
@@ -39,8 +46,12 @@ TAG_GARG = 2
 TAG_GREST = 3
 TAG_RENOISE = 4
 TAG_INIT = 5
+TAG_SEG = 6      # one Exp(1) per vocabulary segment (segmented rule)
+TAG_WITHIN = 7   # one Exp(1) per index, used inside the winning segment
 
 GROUP = 8
+SUPERBLOCK = 1024  # indices per superblock: 32 segments of 4 groups of 8
+SEGMENTS_PER_SUPERBLOCK = 32
 
 _U64 = np.uint64
 _GOLDEN = _U64(0x9E3779B97F4A7C15)
@@ -145,6 +156,21 @@ def gumbel_exponentials(V, ka, kb, kc):
     rest = exp1(draw32(kc, v.astype(np.uint32)))
     is_min = (v - GROUP * g) == j_g[g]
     return x_g[g] / ng[g] + np.where(is_min, 0.0, rest)
+
+
+def segment_of(v):
+    """Segment index of vocabulary index v (vectorised):
+    32 * (v // 1024) + (v mod 256) // 8."""
+    v = np.asarray(v, dtype=np.int64)
+    return SEGMENTS_PER_SUPERBLOCK * (v // SUPERBLOCK) + (v % 256) // GROUP
+
+
+def segment_members(k, V):
+    """The vocabulary indices of segment k, ascending (those < V)."""
+    j, lane = divmod(int(k), SEGMENTS_PER_SUPERBLOCK)
+    v = np.array([SUPERBLOCK * j + 256 * u + GROUP * lane + t
+                  for u in range(4) for t in range(GROUP)], dtype=np.int64)
+    return v[v < V]
 
 
 def gumbel_noise(V, ka, kb, kc):

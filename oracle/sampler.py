@@ -49,6 +49,9 @@ STOP_ENTROPY = 1         # mean entropy below thr for k consecutive steps
 # acceptance rules
 ACCEPT_ENTROPY_BUDGET = 0  # lowest-entropy positions within the entropy budget
 ACCEPT_MONOTONE = 1        # unchanged-or-stronger commits, frozen once committed
+# Gumbel-max sampling rules (both draw the candidate exactly from softmax(y))
+SAMPLE_GROUPED = 0    # argmax(y + G) with per-index G from the group construction
+SAMPLE_SEGMENTED = 1  # a segment by Gumbel-max over segment masses, then an index in it
 
 
 @dataclass
@@ -65,6 +68,7 @@ class Params:
     accept_rule: int = ACCEPT_ENTROPY_BUDGET
     softcap: float = 0.0       # c of the logit softcap; 0 = logits used as stored
     embed_scale: float = 0.0   # factor on the self-conditioning feed; 0 = 1
+    sample_rule: int = SAMPLE_GROUPED
 
 
 @dataclass
@@ -145,9 +149,49 @@ def gumbel_keys(seed, request_id, rng_step, position):
             rng.stream_key(p, rng.TAG_GREST))
 
 
-def vocab_pass(z, T, ka, kb, kc) -> PositionResult:
+def segment_keys(seed, request_id, rng_step, position):
+    """Stream keys (K_SEG, K_WITHIN) of the segmented rule at one position."""
+    p = rng.position_key(seed, request_id, rng_step, position)
+    return rng.stream_key(p, rng.TAG_SEG), rng.stream_key(p, rng.TAG_WITHIN)
+
+
+def segmented_candidate(y, ks, kw):
+    """Hierarchical Gumbel-max (the chunk-level variant of the vLLM blog's
+    argmax(logits/T + gumbel_noise), section "Putting it together").
+
+    Step 1: each segment k (rng.segment_of) has mass W_k = sum_{v in k}
+    exp(y_v - m); the winning segment is argmax_k (ln W_k + G_k), G_k =
+    -ln exp1(draw32(K_SEG, k)) standard Gumbel, lowest k on ties.  By
+    Gumbel-max, P(k) = W_k / sum W.  Step 2: inside it, the candidate is
+    argmax_v (y_v + G'_v), G'_v = -ln exp1(draw32(K_WITHIN, v)), lowest v on
+    ties, so P(v | k) = exp(y_v) / W_k and P(v) = softmax(y)_v exactly.
+    Returns (candidate, gap): gap is the smaller of the two top-2 score gaps
+    (segments, and indices inside the winning segment)."""
+    y = np.asarray(y, dtype=np.float64)
+    V = y.size
+    m = float(np.max(y))
+    e = np.exp(y - m)
+    seg = rng.segment_of(np.arange(V))
+    W = np.bincount(seg, weights=e)
+    k_all = np.arange(W.size)
+    E = rng.exp1(rng.draw32(ks, k_all.astype(np.uint32)))
+    with np.errstate(divide="ignore"):
+        score = np.log(W) - np.log(E)
+    k = int(np.argmax(score))
+    gap_seg = float(score[k] - np.max(np.delete(score, k))) if W.size > 1 else math.inf
+    members = rng.segment_members(k, V)
+    Ew = rng.exp1(rng.draw32(kw, members.astype(np.uint32)))
+    s2 = y[members] - np.log(Ew)
+    i = int(np.argmax(s2))
+    gap_in = float(s2[i] - np.max(np.delete(s2, i))) if members.size > 1 else math.inf
+    return int(members[i]), min(gap_seg, gap_in)
+
+
+def vocab_pass(z, T, ka, kb, kc, sample_rule=SAMPLE_GROUPED, seg_keys=None) -> PositionResult:
     """All per-position quantities of one logit row ``z`` (float64, the stored
-    logits widened exactly) at temperature ``T``.
+    logits widened exactly) at temperature ``T``.  The candidate follows
+    ``sample_rule``: SAMPLE_GROUPED uses the Gumbel keys (ka, kb, kc),
+    SAMPLE_SEGMENTED the segment keys ``seg_keys`` = (K_SEG, K_WITHIN).
 
     Validity (a reading; the pages are silent): a row holding a NaN or a +inf
     logit, a row whose logits are all -inf, or a non-positive / non-finite
@@ -172,6 +216,9 @@ def vocab_pass(z, T, ka, kb, kc) -> PositionResult:
     H = float(-np.sum(p[nz] * np.log(p[nz])))
     # clean argmax, lowest index on ties (vLLM blog: the argmax canvas)
     am = int(np.argmax(z))
+    if sample_rule == SAMPLE_SEGMENTED:
+        cand, gap = segmented_candidate(y, *seg_keys)
+        return PositionResult(True, m, s, H, am, cand, gap)
     # Gumbel-max candidate argmax(y + G), lowest index on ties
     G = rng.gumbel_noise(V, ka, kb, kc)
     score = y + G
@@ -306,9 +353,10 @@ def commit_row(p: Params, st: State, r: int):
 def _vocab_job(args):
     """One position's vocabulary pass (a picklable unit for a process pool).
     The softcap, when set, is applied to the stored logits first."""
-    z, T, seed, rid, rstep, i, cap = args
+    z, T, seed, rid, rstep, i, cap, rule = args
     ka, kb, kc = gumbel_keys(seed, rid, rstep, i)
-    return vocab_pass(softcap(z, cap), T, ka, kb, kc)
+    sk = segment_keys(seed, rid, rstep, i) if rule == SAMPLE_SEGMENTED else None
+    return vocab_pass(softcap(z, cap), T, ka, kb, kc, rule, sk)
 
 
 def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=map):
@@ -317,8 +365,8 @@ def denoise_row(p: Params, st: State, r: int, logits_row, flags: Flags, mapper=m
     process pool's ``map``)."""
     C, V = p.canvas_len, p.vocab
     T = float(st.temperature[r])
-    jobs = [(logits_row[i], T, p.seed, st.request_id[r], st.rng_step[r], i, p.softcap)
-            for i in range(C)]
+    jobs = [(logits_row[i], T, p.seed, st.request_id[r], st.rng_step[r], i, p.softcap,
+             p.sample_rule) for i in range(C)]
     H = np.empty(C)
     for i, res in enumerate(mapper(_vocab_job, jobs)):
         st.m[r, i] = res.m
