@@ -150,8 +150,16 @@ def gpu_id_for(dev) -> str:
 
 # ---------------------------------------------------------- CPU oracle leg
 
+def _oracle_position(osam, z, T, i, rule):
+    """The oracle's vocabulary pass of position i of canvas 0 under ``rule``."""
+    ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
+    sk = osam.segment_keys(SEED, 0, 0, i) if rule == "segmented" else None
+    r = osam.SAMPLE_SEGMENTED if rule == "segmented" else osam.SAMPLE_GROUPED
+    return osam.vocab_pass(z, T, ka, kb, kc, r, sk)
+
+
 def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None = None,
-                      cap: float = 0.0, scale: float = 0.0):
+                      cap: float = 0.0, scale: float = 0.0, rule: str = "grouped"):
     """Time the fp64 oracle on a bounded sample of the workload: P positions of
     canvas 0 (vocabulary pass each, canvas-level acceptance on their
     entropies) plus their self-conditioning rows through one fp64 matmul,
@@ -174,9 +182,8 @@ def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None =
         t0 = time.perf_counter()
         H = []
         for i in range(zrows.shape[0]):
-            ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
             zc = osam.softcap(zrows[i].astype(np.float64), cap)
-            H.append(osam.vocab_pass(zc, Tf, ka, kb, kc).entropy)
+            H.append(_oracle_position(osam, zc, Tf, i, rule).entropy)
         osam.accept_mask(np.resize(np.asarray(H), C), budget)
         osc.selfcond_rows(zrows.astype(np.float64), Tf, E, cap=cap, scale=scale)
         return time.perf_counter() - t0
@@ -196,11 +203,12 @@ def cpu_oracle_sample(wl_name: str, budget_s: float, max_positions: int | None =
 
 
 def cpu_baseline_subprocess(wl_name: str, budget_s: float = 12.0, cap: float = 0.0,
-                            scale: float = 0.0):
+                            scale: float = 0.0, rule: str = "grouped"):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-oracle-leg", "--workload", wl_name,
-           "--cpu-budget", str(budget_s), "--softcap", str(cap), "--embed-scale", str(scale)]
+           "--cpu-budget", str(budget_s), "--softcap", str(cap), "--embed-scale", str(scale),
+           "--sample-rule", rule]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
     for line in r.stdout.splitlines()[::-1]:
         if line.startswith("{"):
@@ -255,7 +263,9 @@ def run_ours(args, rank, world, dev):
                   stop_rule={"argmax": dg.DG_STOP_ARGMAX_STABLE, "entropy": dg.DG_STOP_ENTROPY}[args.stop_rule],
                   accept_rule={"budget": dg.DG_ACCEPT_ENTROPY_BUDGET,
                                "monotone": dg.DG_ACCEPT_MONOTONE}[args.accept_rule],
-                  softcap=args.softcap, embed_scale=args.embed_scale)
+                  softcap=args.softcap, embed_scale=args.embed_scale,
+                  sample_rule={"grouped": dg.DG_SAMPLE_GROUPED,
+                               "segmented": dg.DG_SAMPLE_SEGMENTED}[args.sample_rule])
     logits = syn.boosted_logits(B * C, V, seed=SEED + rank, dtype=tdt, device=dev,
                                 boost_hi=boost).reshape(-1)
     E = syn.embedding(V, d, seed=SEED, device=dev)
@@ -383,7 +393,8 @@ def run_ours(args, rank, world, dev):
                        logit_bytes / 1e9, V * d * 2 / 1e9),
                    "parallelism": f"replicas x{world} (independent requests per GPU)",
                    "accept_rule": args.accept_rule, "stop_rule": args.stop_rule,
-                   "softcap": args.softcap, "embed_scale": args.embed_scale},
+                   "softcap": args.softcap, "embed_scale": args.embed_scale,
+                   "sample_rule": args.sample_rule},
         "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16,
@@ -407,7 +418,8 @@ def run_ours(args, rank, world, dev):
     if not args.no_cpu_baseline:
         try:
             cb = cpu_baseline_subprocess(args.workload if not args.batch else DEFAULT,
-                                         cap=args.softcap, scale=args.embed_scale)
+                                         cap=args.softcap, scale=args.embed_scale,
+                                         rule=args.sample_rule)
             line["cpu_baseline"] = {"value": cb["value"], "unit": "positions/s", "cores": 1,
                                     "kind": "oracle", "sample": cb["sample"]}
         except Exception as e:  # pragma: no cover
@@ -597,7 +609,8 @@ def run_reference(args, rank, world):
     B, C, V, dt, T, budget, d, boost = WORKLOADS[args.workload]
     # each step: a bounded sample sized so the whole run takes ~2-3 minutes
     per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))
-    rate, P, t = cpu_oracle_sample(args.workload, per_step, max_positions=None)
+    rate, P, t = cpu_oracle_sample(args.workload, per_step, max_positions=None,
+                                   rule=args.sample_rule)
     # warm-up + timed steps on the same sample size
     import torch
     from denoise_step_sampler_gb300 import synthetic as syn
@@ -611,8 +624,8 @@ def run_reference(args, rank, world):
     def one():
         H = []
         for i in range(P):
-            ka, kb, kc = osam.gumbel_keys(SEED, 0, 0, i)
-            H.append(osam.vocab_pass(z[i].astype(np.float64), Tf, ka, kb, kc).entropy)
+            H.append(_oracle_position(osam, z[i].astype(np.float64), Tf, i,
+                                      args.sample_rule).entropy)
         osam.accept_mask(np.resize(np.asarray(H), C), budget)
         osc.selfcond_rows(z.astype(np.float64), Tf, E)
 
@@ -659,6 +672,9 @@ def main():
                     help="entropy-budget acceptance or the unchanged-or-stronger commit rule")
     ap.add_argument("--stop-rule", default="argmax", choices=["argmax", "entropy"],
                     help="argmax-stable convergence or the entropy-only stop")
+    ap.add_argument("--sample-rule", default="grouped", choices=["grouped", "segmented"],
+                    help="Gumbel-max rule of the candidate: one Gumbel per index (grouped "
+                         "construction) or the segmented two-level draw")
     ap.add_argument("--anneal", action="store_true",
                     help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop", "mixed-loop"],
@@ -676,6 +692,7 @@ def main():
 
     if args.cpu_oracle_leg:
         rate, P, t = cpu_oracle_sample(args.workload, args.cpu_budget, cap=args.softcap,
+                                       rule=args.sample_rule,
                                        scale=args.embed_scale)
         print(json.dumps({"value": rate, "positions": P, "seconds": t,
                           "sample": f"{P} positions of canvas 0 of the same workload: vocab pass "

@@ -32,6 +32,7 @@ DG_PHASE_PREFILL, DG_PHASE_DENOISE, DG_PHASE_COMMIT, DG_PHASE_IDLE = 0, 1, 2, 3
 DG_F32, DG_BF16 = 0, 1
 DG_STOP_ARGMAX_STABLE, DG_STOP_ENTROPY = 0, 1
 DG_ACCEPT_ENTROPY_BUDGET, DG_ACCEPT_MONOTONE = 0, 1
+DG_SAMPLE_GROUPED, DG_SAMPLE_SEGMENTED = 0, 1
 DG_DEV_NONFINITE_LOGITS, DG_DEV_BAD_TEMPERATURE, DG_DEV_BAD_TOKEN = 1, 2, 4
 DG_DEV_WAIT_TIMEOUT, DG_DEV_BAD_PHASE = 8, 16
 
@@ -50,7 +51,7 @@ class _CParams(ctypes.Structure):
         ("conf_threshold", ctypes.c_float), ("stable_k", ctypes.c_int32),
         ("step_cap", ctypes.c_int32), ("stop_rule", ctypes.c_int32),
         ("accept_rule", ctypes.c_int32), ("softcap", ctypes.c_float),
-        ("embed_scale", ctypes.c_float),
+        ("embed_scale", ctypes.c_float), ("sample_rule", ctypes.c_int32),
     ]
 
 
@@ -126,13 +127,14 @@ class Params:
     accept_rule: int = DG_ACCEPT_ENTROPY_BUDGET
     softcap: float = 0.0      # logit softcap c (0 = off)
     embed_scale: float = 0.0  # factor on the self-conditioning feed (0 = 1)
+    sample_rule: int = DG_SAMPLE_GROUPED  # Gumbel-max rule of the candidate
 
     def c(self) -> _CParams:
         return _CParams(self.batch, self.canvas_len, self.vocab, self.logits_dtype,
                         self.vocab if self.logits_ld is None else self.logits_ld,
                         self.seed & 0xFFFFFFFFFFFFFFFF, self.entropy_budget,
                         self.conf_threshold, self.stable_k, self.step_cap, self.stop_rule,
-                        self.accept_rule, self.softcap, self.embed_scale)
+                        self.accept_rule, self.softcap, self.embed_scale, self.sample_rule)
 
 
 class State:

@@ -25,6 +25,7 @@ bool params_ok(const dg_params *p) {
     return false;
   if (!std::isfinite(p->softcap) || p->softcap < 0.f) return false;
   if (!std::isfinite(p->embed_scale) || p->embed_scale < 0.f) return false;
+  if (p->sample_rule != DG_SAMPLE_GROUPED && p->sample_rule != DG_SAMPLE_SEGMENTED) return false;
   // positions and partial records must be addressable
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
   if (n_pos > ((int64_t)1 << 40)) return false;

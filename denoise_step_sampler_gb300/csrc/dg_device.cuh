@@ -14,7 +14,11 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kGroup = 8;  // vocabulary indices per Gumbel group
 
-enum : uint32_t { kTagGMin = 1, kTagGArg = 2, kTagGRest = 3, kTagRenoise = 4, kTagInit = 5 };
+enum : uint32_t {
+  kTagGMin = 1, kTagGArg = 2, kTagGRest = 3, kTagRenoise = 4, kTagInit = 5,
+  kTagSeg = 6,     // segmented rule: one draw per vocabulary segment
+  kTagWithin = 7   // segmented rule: one draw per index of the winning segment
+};
 
 // SplitMix64 output function of the state x (Steele, Lea & Flood 2014).
 __host__ __device__ __forceinline__ uint64_t mix64(uint64_t x) {
@@ -118,7 +122,7 @@ enum : uint32_t { kPartNaN = 1u, kPartPInf = 2u, kPartBadT = 4u };
 // Chunking of the vocabulary for the vocabulary pass: a pure function of the
 // sizes, shared by the workspace query and the launch.
 struct VocabChunking {
-  int32_t chunk;     // elements per chunk (multiple of 256 unless one chunk)
+  int32_t chunk;     // elements per chunk (a multiple of 1024)
   int32_t n_chunks;  // chunks per position
 };
 __host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V) {
@@ -133,8 +137,11 @@ __host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V
   if (n_pos <= 9728) nc = 4;
   if (n_pos <= 1216) nc = 8;
   while (nc > 1 && ((int64_t)V + nc - 1) / nc < 2048) nc >>= 1;
+  // chunks start on multiples of 1024 indices, so that every vocabulary
+  // segment of the segmented Gumbel-max rule (32 indices inside one
+  // superblock of 1024) lies in one chunk
   int64_t chunk = ((int64_t)V + nc - 1) / nc;
-  chunk = (chunk + 255) / 256 * 256;
+  chunk = (chunk + 1023) / 1024 * 1024;
   VocabChunking out;
   out.chunk = (int32_t)chunk;
   out.n_chunks = (int32_t)(((int64_t)V + chunk - 1) / chunk);

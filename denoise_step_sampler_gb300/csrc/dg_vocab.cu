@@ -27,6 +27,7 @@ constexpr int kWarps = 8;  // warps per CTA
 
 struct Keys {
   uint32_t ka, kb, kc;  // low words of the GMIN / GARG / GREST stream keys
+  uint32_t ks, kw;      // low words of the SEG / WITHIN stream keys (segmented rule)
 };
 
 // The softmax sums are kept in three levels so that no fp32 sum adds more
@@ -44,8 +45,10 @@ struct Lane {
   float2 S0, S1, T0, T1;        // round sums of 2^a and a 2^a, in pairs
   float2 BS, BT;                // block sums
   float ts, tt;                 // chunk totals
-  float b2;     // best perturbed score, base 2
-  int32_t cand;
+  float b2;     // best perturbed score, base 2 (segmented rule: best segment score)
+  int32_t cand;  // its index (segmented rule: the segment's id until the inner draw)
+  float pseg;   // segmented rule: sum of 2^a over the pending segment, reference m2
+  int32_t pk;   // segmented rule: pending segment id (-1 none)
 };
 
 __device__ __forceinline__ void lane_init(Lane &L) {
@@ -57,6 +60,8 @@ __device__ __forceinline__ void lane_init(Lane &L) {
   L.ts = L.tt = 0.f;
   L.b2 = -INFINITY;
   L.cand = -1;
+  L.pseg = 0.f;
+  L.pk = -1;
 }
 
 // Round sums into the block sums.
@@ -86,6 +91,7 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
     L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
     L.BS = L.BT = make_float2(0.f, 0.f);
     L.ts = L.tt = 0.f;
+    L.pseg = 0.f;
     L.m2 = m2n;
     return;
   }
@@ -102,7 +108,42 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
   one(L.BS, L.BT);
   L.tt = fmaf(d, L.ts, L.tt) * f;
   L.ts *= f;
+  L.pseg *= f;
   L.m2 = m2n;
+}
+
+// ---- segmented Gumbel-max rule ("DiffusionGemma: the first dLLM natively
+// supported in vLLM", "Putting it together": argmax(logits/T + gumbel_noise),
+// drawn in two levels).  Segment k = 32 j + l holds the indices
+// 1024 j + 256 u + 8 l + t (u < 4, t < 8), so the 8-index group g lies in
+// segment 32 (g >> 7) + (g & 31): with chunks starting on multiples of 1024,
+// lane l of a warp only ever sees groups of its own segments.
+
+__device__ __forceinline__ int32_t segment_of_group(uint32_t g) {
+  return (int32_t)(32u * (g >> 7) + (g & 31u));
+}
+
+// Score the pending segment: its base-2 score m2 + log2(sum 2^a) - log2(E_k),
+// E_k = X(draw32(K_SEG, k)); keep the best (lowest id on ties).
+__device__ __forceinline__ void seg_close(Lane &L, const Keys &K) {
+  if (L.pk >= 0 && L.pseg > 0.f) {
+    const float E = exp1_draw(fmix32(K.ks ^ (uint32_t)L.pk));
+    const float sc = L.m2 + (__log2f(L.pseg) - __log2f(E));
+    if (sc > L.b2 || (sc == L.b2 && L.pk < L.cand)) {
+      L.b2 = sc;
+      L.cand = L.pk;
+    }
+  }
+  L.pk = -1;
+  L.pseg = 0.f;
+}
+// Add the mass (relative to L.m2) of some indices of segment k.
+__device__ __forceinline__ void seg_add(Lane &L, int32_t k, float mass, const Keys &K) {
+  if (k != L.pk) {
+    seg_close(L, K);
+    L.pk = k;
+  }
+  L.pseg += mass;
 }
 
 // Rounds of the bf16 path stream through a per-warp ring in shared memory
@@ -196,6 +237,45 @@ __device__ __forceinline__ bool group8(const float (&z)[8], uint32_t g, float c,
   const float w = (float)(~h) * 2.3283064365386963e-10f;
   const float thr = 8.0f * ex2_approx(fmaf(vmax, c, -sb));
   return w <= thr * 1.001f;
+}
+
+// The segmented rule's form of group8: max / argmax and the softmax sums of a
+// full group of 8 finite logits; returns the group's mass sum 2^(z c - m2)
+// (no Gumbel screen: the rule draws once per segment).
+__device__ __forceinline__ float group8_seg(const float (&z)[8], uint32_t g, float c, Lane &L) {
+  const float vmax = fmaxf(fmaxf(fmaxf(z[0], z[1]), fmaxf(z[2], z[3])),
+                           fmaxf(fmaxf(z[4], z[5]), fmaxf(z[6], z[7])));
+  if (vmax > L.zmax) {
+    int j = 7;
+#pragma unroll
+    for (int jj = 6; jj >= 0; --jj)
+      if (z[jj] == vmax) j = jj;
+    const float m2n = vmax * c;
+    rescale(L, m2n);
+    L.zmax = vmax;
+    L.am = (int32_t)(g * kGroup + j);
+    L.m2 = m2n;
+  }
+  const float2 cc = make_float2(c, c);
+  const float2 mm = make_float2(-L.m2, -L.m2);
+  const float2 a0 = __ffma2_rn(make_float2(z[0], z[1]), cc, mm);
+  const float2 a1 = __ffma2_rn(make_float2(z[2], z[3]), cc, mm);
+  const float2 a2 = __ffma2_rn(make_float2(z[4], z[5]), cc, mm);
+  const float2 a3 = __ffma2_rn(make_float2(z[6], z[7]), cc, mm);
+  const float2 e0 = make_float2(ex2_approx(a0.x), ex2_approx(a0.y));
+  const float2 e1 = make_float2(ex2_approx(a1.x), ex2_approx(a1.y));
+  const float2 e2 = make_float2(ex2_approx(a2.x), ex2_approx(a2.y));
+  const float2 e3 = make_float2(ex2_approx(a3.x), ex2_approx(a3.y));
+  L.S0 = __fadd2_rn(L.S0, e0);
+  L.S1 = __fadd2_rn(L.S1, e1);
+  L.T0 = __ffma2_rn(a0, e0, L.T0);
+  L.T1 = __ffma2_rn(a1, e1, L.T1);
+  L.S0 = __fadd2_rn(L.S0, e2);
+  L.S1 = __fadd2_rn(L.S1, e3);
+  L.T0 = __ffma2_rn(a2, e2, L.T0);
+  L.T1 = __ffma2_rn(a3, e3, L.T1);
+  const float2 es = __fadd2_rn(__fadd2_rn(e0, e1), __fadd2_rn(e2, e3));
+  return es.x + es.y;
 }
 
 // Exact evaluation of the groups that passed the screen, deferred through a
@@ -304,7 +384,9 @@ __device__ __forceinline__ void share_bound(int32_t *slot, float &wb, int lane) 
 }
 
 // Careful path for any group (n <= 8 members, any values): flags NaN / +inf,
-// skips -inf, evaluates every finite member's Gumbel score exactly.
+// skips -inf, evaluates every finite member's Gumbel score exactly (grouped
+// rule) or adds the group's mass to its segment (segmented rule).
+template <bool SEG>
 __device__ void group_careful(const float *z, int n, uint32_t g, float c, const Keys &K, Lane &L,
                               uint32_t &flags) {
   float zz[8];
@@ -344,7 +426,10 @@ __device__ void group_careful(const float *z, int n, uint32_t g, float c, const 
   L.S0.x += s;
   L.T0.x += t;
   if ((g & 15u) == 15u) fold_block(L); else fold_round(L);
-  gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, L.b2, K, L);
+  if constexpr (SEG)
+    seg_add(L, segment_of_group(g), s, K);
+  else
+    gumbel_group_exact(zz, n, g, fmix32(K.ka ^ g), c, L.b2, K, L);
 }
 
 // Largest of the 32 bf16 values of a round (NaN values are ignored; the sums
@@ -473,9 +558,42 @@ __device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32
   }
 }
 
-// CAP: logits pass through the softcap (cap_k = 2 log2(e) / c, cap_c = c)
-// before any other use; capped calls take the per-group path.
+// The segmented rule's inner draw: the warp's best segment k (warp-uniform)
+// has 32 indices, one per lane; the candidate is the index maximising
+// z c - log2(E_v), E_v = X(draw32(K_WITHIN, v)), lowest index on ties.
 template <int DT, bool CAP>
+__device__ __forceinline__ int32_t segment_inner_draw(const void *row, int32_t V, int32_t k,
+                                                      float c, const Keys &K, float cap_k,
+                                                      float cap_c, int lane) {
+  const int64_t v = 1024 * (int64_t)(k >> 5) + 256 * (lane >> 3) + 8 * (k & 31) + (lane & 7);
+  float sc = -INFINITY;
+  int32_t idx = -1;
+  if (v < V) {
+    float z = load_scalar<DT>(row, v);
+    if (CAP) z = softcap_f(z, cap_k, cap_c);
+    if (z > -INFINITY && z < INFINITY) {
+      const float E = exp1_draw(fmix32(K.kw ^ (uint32_t)v));
+      sc = fmaf(z, c, -__log2f(E));
+      idx = (int32_t)v;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float os = __shfl_xor_sync(0xFFFFFFFFu, sc, off);
+    const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, idx, off);
+    if (os > sc || (os == sc && oi >= 0 && (idx < 0 || oi < idx))) {
+      sc = os;
+      idx = oi;
+    }
+  }
+  return idx;
+}
+
+// CAP: logits pass through the softcap (cap_k = 2 log2(e) / c, cap_c = c)
+// before any other use; capped calls take the per-group path.  SEG: the
+// candidate follows the segmented rule (no Gumbel screen, queue or shared
+// bound; one draw per segment of 32 indices, then the inner draw).
+template <int DT, bool CAP, bool SEG>
 // The bf16 ring path runs 3 CTAs of 8 warps per SM (the ring and the queues
 // fill shared memory), at most 80 registers per thread; the other paths 4 CTAs
 // at 64.
@@ -487,7 +605,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
                       const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
                       Partial *__restrict__ part, uint32_t *__restrict__ status) {
   __shared__ int32_t s_bound[kWarps];  // best score per position handled by this CTA
-  __shared__ QEntry s_queue[kWarps][kQueue];
+  __shared__ QEntry s_queue[kWarps][SEG ? 1 : kQueue];
   extern __shared__ uint4 s_ring[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -529,6 +647,10 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
   K.ka = (uint32_t)stream_key(pk, kTagGMin);
   K.kb = (uint32_t)stream_key(pk, kTagGArg);
   K.kc = (uint32_t)stream_key(pk, kTagGRest);
+  if constexpr (SEG) {
+    K.ks = (uint32_t)stream_key(pk, kTagSeg);
+    K.kw = (uint32_t)stream_key(pk, kTagWithin);
+  }
 
   const int64_t v0 = (int64_t)ch * chunk;
   const int64_t v1 = min((int64_t)V, v0 + chunk);
@@ -563,7 +685,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
     // groups.
     const float2 cc = make_float2(c, c);
     int am_round = -1;
-    if (rounds > 0) {
+    if (!SEG && rounds > 0) {
       // Warm start: each lane scores the largest logit of its first round
       // exactly, so that the first round is already screened against a
       // finite bound instead of queueing every group.
@@ -642,6 +764,15 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
           }
         }
       }
+      if constexpr (SEG) {
+        // the round is lane's whole segment of superblock (v0 / 1024 + rd):
+        // its mass is the round's sums, scored at once
+        const float2 es = __fadd2_rn(L.S0, L.S1);
+        seg_add(L, (int32_t)(32u * (uint32_t)(v0 / 1024 + rd) + (uint32_t)lane), es.x + es.y, K);
+        seg_close(L, K);
+        if ((rd & 15) == 15) fold_block(L); else fold_round(L);
+        continue;
+      }
       // Gumbel screen: group g can hold a score >= wb only if its W_g
       // (= (~h + 1/2) 2^-32) <= 8 2^(vmax c - wb); with the round maximum for
       // vmax and a 0.1 % margin that is ~h <= 2^(rmax c - wb + 35.00144).
@@ -684,6 +815,14 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
       float z[8];
       uint32_t h = 0;
       bool pass = false;
+      if constexpr (SEG) {
+        if (q < n_full) {
+          unpack_bf16x8(ld_stream(vrow + q), z);
+          const uint32_t g = g0 + (uint32_t)q;
+          seg_add(L, segment_of_group(g), group8_seg(z, g, c, L), K);
+        }
+        continue;
+      }
       if (q < n_full) {
         unpack_bf16x8(ld_stream(vrow + q), z);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
@@ -708,12 +847,16 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
                       __uint_as_float(v[2 * u + 1].x), __uint_as_float(v[2 * u + 1].y),
                       __uint_as_float(v[2 * u + 1].z), __uint_as_float(v[2 * u + 1].w)};
         const uint32_t g = g0 + (uint32_t)(q + u * 32);
-        uint32_t h;
-        const bool pass = group8(z, g, c, wb, K, L, h);
-        coop_eval(pass, z, g, h, c, wb, K, L, lane, Q);
+        if constexpr (SEG) {
+          seg_add(L, segment_of_group(g), group8_seg(z, g, c, L), K);
+        } else {
+          uint32_t h;
+          const bool pass = group8(z, g, c, wb, K, L, h);
+          coop_eval(pass, z, g, h, c, wb, K, L, lane, Q);
+        }
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
-      share_bound(slot, wb, lane);
+      if (!SEG) share_bound(slot, wb, lane);
     }
     for (int base = rounds * 64; base < n_full; base += 32) {
       const int q = base + lane;
@@ -726,9 +869,12 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
         z[2] = __uint_as_float(a.z); z[3] = __uint_as_float(a.w);
         z[4] = __uint_as_float(b.x); z[5] = __uint_as_float(b.y);
         z[6] = __uint_as_float(b.z); z[7] = __uint_as_float(b.w);
-        pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
+        if constexpr (SEG)
+          seg_add(L, segment_of_group(g0 + (uint32_t)q), group8_seg(z, g0 + (uint32_t)q, c, L), K);
+        else
+          pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
+      if (!SEG) coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
     }
   } else {
     for (int base = 0; base < n_full; base += 32) {  // warp-uniform trip count
@@ -738,15 +884,18 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
       bool pass = false;
       if (q < n_full) {
         load_group<DT, CAP>(row, aligned, v0 + (int64_t)q * kGroup, 8, z, cap_k, cap_c);
-        pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
+        if constexpr (SEG)
+          seg_add(L, segment_of_group(g0 + (uint32_t)q), group8_seg(z, g0 + (uint32_t)q, c, L), K);
+        else
+          pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
-      coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
+      if (!SEG) coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
       if ((base & 511) == 480) fold_block(L); else if ((base & 127) == 96) fold_round(L);
-      if ((base & 127) == 96) share_bound(slot, wb, lane);
+      if (!SEG && (base & 127) == 96) share_bound(slot, wb, lane);
     }
   }
 
-  flush_queue(Q, c, wb, K, L, lane);
+  if (!SEG) flush_queue(Q, c, wb, K, L, lane);
   float s, t;
   sums(L, s, t);
   const bool bad = !(isfinite(s) && isfinite(t));
@@ -756,19 +905,24 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
     for (int q = lane; q < n_full; q += 32) {
       float z[8];
       load_group<DT, CAP>(row, aligned, v0 + (int64_t)q * kGroup, 8, z, cap_k, cap_c);
-      group_careful(z, 8, g0 + (uint32_t)q, c, K, L, flags);
+      group_careful<SEG>(z, 8, g0 + (uint32_t)q, c, K, L, flags);
     }
   }
   if (tail_n > 0 && lane == (n_full & 31)) {
     float z[8];
     load_group<DT, CAP>(row, false, v0 + (int64_t)n_full * kGroup, tail_n, z, cap_k, cap_c);
-    group_careful(z, tail_n, g0 + (uint32_t)n_full, c, K, L, flags);
+    group_careful<SEG>(z, tail_n, g0 + (uint32_t)n_full, c, K, L, flags);
   }
   sums(L, s, t);
+  if (SEG) seg_close(L, K);
 
   float zmax = L.zmax, b2 = L.b2;
   int32_t am = L.am, cand = L.cand;
   warp_merge(c, L.m2, zmax, am, s, t, b2, cand);
+  // segmented rule: cand is the warp's best segment (warp-uniform after the
+  // merge); draw the index inside it
+  if (SEG && b2 > -INFINITY)
+    cand = segment_inner_draw<DT, CAP>(row, V, cand, c, K, cap_k, cap_c, lane);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, off);
   if (lane == 0) {
@@ -799,7 +953,10 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false>,
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
@@ -808,16 +965,28 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const bool cap = p.softcap > 0.f;
   const float cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
   const float cap_c = cap ? p.softcap : 0.f;
-#define DG_VOCAB_LAUNCH(DT, CAP)                                                              \
-  vocab_pass_kernel<DT, CAP><<<(unsigned)blocks, kWarps * 32, (DT == DG_BF16 && !CAP) ? kRingBytes : 0, s>>>( \
+#define DG_VOCAB_LAUNCH(DT, CAP, SEG)                                                         \
+  vocab_pass_kernel<DT, CAP, SEG><<<(unsigned)blocks, kWarps * 32,                           \
+                                    (DT == DG_BF16 && !CAP) ? kRingBytes : 0, s>>>(          \
       logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c, \
       st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status)
+  const bool seg = p.sample_rule == DG_SAMPLE_SEGMENTED;
   if (p.logits_dtype == DG_BF16) {
-    if (cap) DG_VOCAB_LAUNCH(DG_BF16, true);
-    else DG_VOCAB_LAUNCH(DG_BF16, false);
+    if (cap) {
+      if (seg) DG_VOCAB_LAUNCH(DG_BF16, true, true);
+      else DG_VOCAB_LAUNCH(DG_BF16, true, false);
+    } else {
+      if (seg) DG_VOCAB_LAUNCH(DG_BF16, false, true);
+      else DG_VOCAB_LAUNCH(DG_BF16, false, false);
+    }
   } else {
-    if (cap) DG_VOCAB_LAUNCH(DG_F32, true);
-    else DG_VOCAB_LAUNCH(DG_F32, false);
+    if (cap) {
+      if (seg) DG_VOCAB_LAUNCH(DG_F32, true, true);
+      else DG_VOCAB_LAUNCH(DG_F32, true, false);
+    } else {
+      if (seg) DG_VOCAB_LAUNCH(DG_F32, false, true);
+      else DG_VOCAB_LAUNCH(DG_F32, false, false);
+    }
   }
 #undef DG_VOCAB_LAUNCH
   return cudaGetLastError();

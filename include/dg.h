@@ -87,6 +87,22 @@ enum { DG_STOP_ARGMAX_STABLE = 0, DG_STOP_ENTROPY = 1 };
  *   and the last candidates elsewhere.  Needs dg_state.committed / prev_conf. */
 enum { DG_ACCEPT_ENTROPY_BUDGET = 0, DG_ACCEPT_MONOTONE = 1 };
 
+/* Gumbel-max sampling rules for the candidate (dg_params.sample_rule).  Both
+ * draw the candidate exactly from softmax(z/T) (vLLM blog, "Putting it
+ * together": argmax(logits/T + gumbel_noise)); they use different random
+ * numbers, so their candidates differ draw by draw.
+ * DG_SAMPLE_GROUPED: argmax_v(z_v/T + G_v) with one Gumbel per index, from
+ *   the library's group construction (8 indices share one minimum draw).
+ * DG_SAMPLE_SEGMENTED: the chunk-level variant.  The vocabulary is cut into
+ *   segments of 32 indices (superblock j = [1024 j, 1024 j + 1024); its
+ *   segment l holds the four groups of 8 at offsets 8 l + 256 u, u < 4).  A
+ *   segment wins by Gumbel-max over ln(sum of its exp(z/T)) with one Gumbel
+ *   per segment; the candidate is the Gumbel-max index inside it (one Gumbel
+ *   per index of that segment only).  By the max-stability of the Gumbel law
+ *   the result has the same distribution; the pass hashes once per 32
+ *   indices instead of screening every group of 8. */
+enum { DG_SAMPLE_GROUPED = 0, DG_SAMPLE_SEGMENTED = 1 };
+
 /* Scalar parameters of a call (host memory, read during the call only). */
 typedef struct {
   int32_t batch;          /* B >= 1 request slots                                */
@@ -111,6 +127,7 @@ typedef struct {
                              embedding scale on the probability-weighted
                              embedding, "The Annotated DiffusionGemma", the
                              forward pass); 0 = 1; finite, >= 0                 */
+  int32_t sample_rule;    /* DG_SAMPLE_* (0 = grouped)                           */
 } dg_params;
 
 /* Per-request state: device arrays, preallocated by the caller and updated in

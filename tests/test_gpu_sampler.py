@@ -46,11 +46,16 @@ CASES = [
 ]
 
 
+RULES = [dg.DG_SAMPLE_GROUPED, dg.DG_SAMPLE_SEGMENTED]
+
+
+@pytest.mark.parametrize("rule", RULES, ids=["grouped", "segmented"])
 @pytest.mark.parametrize("case", CASES, ids=[f"B{c[0]}C{c[1]}V{c[2]}dt{c[3]}ld{c[4]}" for c in CASES])
-def test_denoise_step_matches_oracle(case):
+def test_denoise_step_matches_oracle(case, rule):
     B, C, V, dt, ld, budget, T = case
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dt, logits_ld=ld, seed=0xD1FF0001,
-                  entropy_budget=budget, conf_threshold=0.3, stable_k=3, step_cap=32)
+                  entropy_budget=budget, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  sample_rule=rule)
     st = make_state(p, [dg.DG_PHASE_DENOISE] * B, request_ids=np.arange(B) + 17, temperatures=T,
                     rng_step=np.arange(B) * 5)
     logits = _logits(B, C, V, dt, seed=B * 1000 + V, ld=ld)
@@ -78,10 +83,12 @@ def test_mixed_phases_in_one_batch():
     assert after["num_sampled"].tolist() == [0, 0, C, 0, 0, C]
 
 
-def test_nonfinite_and_masked_rows():
+@pytest.mark.parametrize("rule", RULES, ids=["grouped", "segmented"])
+def test_nonfinite_and_masked_rows(rule):
     B, C, V = 3, 16, 700
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_F32, seed=3,
-                  entropy_budget=10.0, conf_threshold=0.3, stable_k=1, step_cap=8)
+                  entropy_budget=10.0, conf_threshold=0.3, stable_k=1, step_cap=8,
+                  sample_rule=rule)
     st = make_state(p, [1, 1, 1], temperatures=[1.0, 1.0, 0.0])
     logits = _logits(B, C, V, dg.DG_F32, seed=5).view(B, C, V)
     logits[0, 1, 10] = float("nan")
@@ -144,12 +151,14 @@ def test_bad_token_and_phase_set_status_without_trapping():
     assert np.all(snap["emitted"][:C] == 0)
 
 
-def test_multistep_loop_until_every_request_commits():
+@pytest.mark.parametrize("rule", RULES, ids=["grouped", "segmented"])
+def test_multistep_loop_until_every_request_commits(rule):
     """A mixed-phase loop (prefill, denoise, commit requests) with rising
     confidence; every step is compared from the GPU's prior state."""
     B, C, V = 6, 64, 1000
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=0xD1FF0003,
-                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=12)
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=12,
+                  sample_rule=rule)
     temps = syn.temperatures(B, seed=3, device="cpu").numpy()
     phases = [0, 0, 1, 1, 1, 2]
     st = make_state(p, phases, request_ids=np.arange(B), temperatures=temps)
@@ -166,14 +175,16 @@ def test_multistep_loop_until_every_request_commits():
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("rule", RULES, ids=["grouped", "segmented"])
 @pytest.mark.parametrize("T", [1.0, 0.5])
-def test_large_logit_jumps_move_the_sum_reference(T):
+def test_large_logit_jumps_move_the_sum_reference(T, rule):
     """Spikes far above the running maximum (more than 2^32 in base 2) at early,
     middle and late vocabulary indices force the vocabulary pass to move the
     reference of its softmax sums mid-chunk; the results must still match."""
     B, C, V = 1, 16, 262144
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=99,
-                  entropy_budget=8.0, conf_threshold=0.3, stable_k=3, step_cap=32)
+                  entropy_budget=8.0, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  sample_rule=rule)
     logits = _logits(B, C, V, dg.DG_BF16, seed=7).view(B, C, V)
     g = torch.Generator(device="cpu").manual_seed(5)
     for i in range(C):

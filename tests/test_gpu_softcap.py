@@ -36,12 +36,15 @@ STEP_CASES = [
 ]
 
 
+@pytest.mark.parametrize("rule", [dg.DG_SAMPLE_GROUPED, dg.DG_SAMPLE_SEGMENTED],
+                         ids=["grouped", "segmented"])
 @pytest.mark.parametrize("case", STEP_CASES,
                          ids=[f"V{c[2]}-{'bf16' if c[3] else 'f32'}-ld{c[4]}-c{c[5]}" for c in STEP_CASES])
-def test_softcap_step_matches_oracle(case):
+def test_softcap_step_matches_oracle(case, rule):
     B, C, V, dt, ld, cap = case
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dt, logits_ld=ld, seed=0xD1FF0011,
-                  entropy_budget=0.25 * C, conf_threshold=0.3, stable_k=2, step_cap=8, softcap=cap)
+                  entropy_budget=0.25 * C, conf_threshold=0.3, stable_k=2, step_cap=8, softcap=cap,
+                  sample_rule=rule)
     st = make_state(p, [dg.DG_PHASE_DENOISE] * B, request_ids=np.arange(B) + 5,
                     temperatures=np.linspace(0.7, 1.2, B))
     tdt = torch.bfloat16 if dt == dg.DG_BF16 else torch.float32
