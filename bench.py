@@ -238,6 +238,10 @@ def aggregate(ms_local, world, positions_per_step, steps, dist=None, device=None
 
 # ---------------------------------------------------------------- our arm
 
+def _rule(dg, args):
+    return {"grouped": dg.DG_SAMPLE_GROUPED, "segmented": dg.DG_SAMPLE_SEGMENTED}[args.sample_rule]
+
+
 def run_ours(args, rank, world, dev):
     import torch
     import torch.distributed as dist
@@ -264,8 +268,7 @@ def run_ours(args, rank, world, dev):
                   accept_rule={"budget": dg.DG_ACCEPT_ENTROPY_BUDGET,
                                "monotone": dg.DG_ACCEPT_MONOTONE}[args.accept_rule],
                   softcap=args.softcap, embed_scale=args.embed_scale,
-                  sample_rule={"grouped": dg.DG_SAMPLE_GROUPED,
-                               "segmented": dg.DG_SAMPLE_SEGMENTED}[args.sample_rule])
+                  sample_rule=_rule(dg, args))
     logits = syn.boosted_logits(B * C, V, seed=SEED + rank, dtype=tdt, device=dev,
                                 boost_hi=boost).reshape(-1)
     E = syn.embedding(V, d, seed=SEED, device=dev)
@@ -450,7 +453,8 @@ def run_graph_loop(args, dev):
     C, V, d, steps = 256, 262144, 2816, 24
     seed = 0xD1FF0005
     p = dg.Params(batch=1, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=seed,
-                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=steps)
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=steps,
+                  sample_rule=_rule(dg, args))
     T = float(syn.temperatures(1, seed=seed, device="cpu")[0])
     bufs = [syn.loop_logits(C, V, seed=seed, request=0, step=s, device=dev).reshape(-1)
             for s in range(steps + 1)]
@@ -510,6 +514,7 @@ def run_graph_loop(args, dev):
             "higher_is_better": False, "eager_us_per_step": eager_ms / calls * 1e3,
             "graph_ms_per_block": graph_ms, "eager_ms_per_block": eager_ms, "blocks": reps,
             "config": {"workload": "1x256-V262144-bf16-d2816 loop", "steps": steps,
+                       "sample_rule": args.sample_rule,
                        "cap": steps, "temperature": T if not args.anneal else
                        {"anneal": "linear", "t_max": 1.2, "t_min": 0.6, "n_steps": steps}},
             "anneal_us_per_call": anneal_us,
@@ -535,7 +540,8 @@ def run_mixed_loop(args, dev):
     B, C, V, d = 32, 256, 262144, 2816
     seed = 0xD1FF0003
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=seed,
-                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=32)
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  sample_rule=_rule(dg, args))
     temps = syn.temperatures(B, seed=seed, device="cpu")
     phases = torch.tensor([dg.DG_PHASE_PREFILL] * 8 + [dg.DG_PHASE_DENOISE] * 20 +
                           [dg.DG_PHASE_COMMIT] * 4, dtype=torch.uint8)
@@ -594,6 +600,7 @@ def run_mixed_loop(args, dev):
             "every_request_committed": done, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "mixed-32 loop (8 prefill / 20 denoise / 4 commit) "
                                    "V262144-bf16-d2816", "cap": 32, "stable_k": 3,
+                       "sample_rule": args.sample_rule,
                        "conf_threshold": 0.3, "entropy_budget": 96.0,
                        "temperature": "U[0.6, 1.2] per request",
                        "l2": "inputs larger than L2 (up to 2.68 GB of denoise logits a step)"},
@@ -672,9 +679,10 @@ def main():
                     help="entropy-budget acceptance or the unchanged-or-stronger commit rule")
     ap.add_argument("--stop-rule", default="argmax", choices=["argmax", "entropy"],
                     help="argmax-stable convergence or the entropy-only stop")
-    ap.add_argument("--sample-rule", default="grouped", choices=["grouped", "segmented"],
-                    help="Gumbel-max rule of the candidate: one Gumbel per index (grouped "
-                         "construction) or the segmented two-level draw")
+    ap.add_argument("--sample-rule", default="segmented", choices=["grouped", "segmented"],
+                    help="Gumbel-max rule of the candidate: the segmented two-level draw "
+                         "(default, the faster pass) or one Gumbel per index (grouped "
+                         "construction); both draw exactly from softmax(z/T)")
     ap.add_argument("--anneal", action="store_true",
                     help="graph-loop: anneal the temperature 1.2 -> 0.6 on the device each step")
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop", "mixed-loop"],
