@@ -68,6 +68,25 @@ __device__ __forceinline__ float exp1_draw(uint32_t h) {
   return -log1pf(-w);
 }
 
+// The same Exp(1) draw -ln((h + 1/2) / 2^32) without a divergent branch, for
+// code where every lane draws at once (a warp would otherwise run both sides
+// of exp1_draw's branch).  x is the smaller of U and its complement W = 1 - U
+// (both exact multiples of 2^-33 up to fp32 rounding, at most 1/2):
+//   U <= 1/2:  -ln U = -ln 2 * log2 x;
+//   U >  1/2:  -ln(1 - W) = W + W^2/2 + W^3/3 + W^4/4 + W^5/5 + ... for
+//              W <= 1/16 (truncated after five terms: relative error below
+//              W^5 / 6 <= 2^-22), else -ln 2 * log2(1 - W), where 1 - W >= 1/2.
+// Relative error a few 1e-6 at worst (the fast log2 near 1), against the
+// 1e-4 near-tie window of the scores it enters.
+__device__ __forceinline__ float exp1_draw_uniform(uint32_t h) {
+  const bool upper = h >= 0x80000000u;
+  const float x = fmaf((float)(upper ? ~h : h), 2.3283064365386963e-10f, 1.1641532182693481e-10f);
+  const float big = -kLn2 * __log2f(upper ? 1.0f - x : x);
+  const float series =
+      x * fmaf(x, fmaf(x, fmaf(x, fmaf(x, 0.2f, 0.25f), 0.33333334f), 0.5f), 1.0f);
+  return (upper && x <= 0.0625f) ? series : big;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

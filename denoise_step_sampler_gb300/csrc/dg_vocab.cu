@@ -127,7 +127,7 @@ __device__ __forceinline__ int32_t segment_of_group(uint32_t g) {
 // E_k = X(draw32(K_SEG, k)); keep the best (lowest id on ties).
 __device__ __forceinline__ void seg_close(Lane &L, const Keys &K) {
   if (L.pk >= 0 && L.pseg > 0.f) {
-    const float E = exp1_draw(fmix32(K.ks ^ (uint32_t)L.pk));
+    const float E = exp1_draw_uniform(fmix32(K.ks ^ (uint32_t)L.pk));
     const float sc = L.m2 + (__log2f(L.pseg) - __log2f(E));
     if (sc > L.b2 || (sc == L.b2 && L.pk < L.cand)) {
       L.b2 = sc;
@@ -572,7 +572,7 @@ __device__ __forceinline__ int32_t segment_inner_draw(const void *row, int32_t V
     float z = load_scalar<DT>(row, v);
     if (CAP) z = softcap_f(z, cap_k, cap_c);
     if (z > -INFINITY && z < INFINITY) {
-      const float E = exp1_draw(fmix32(K.kw ^ (uint32_t)v));
+      const float E = exp1_draw_uniform(fmix32(K.kw ^ (uint32_t)v));
       sc = fmaf(z, c, -__log2f(E));
       idx = (int32_t)v;
     }
