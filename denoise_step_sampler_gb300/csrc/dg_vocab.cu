@@ -468,6 +468,16 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&z)[8]) {
   z[7] = __uint_as_float(v.w & 0xFFFF0000u);
 }
 
+// unpack_bf16x8, then (CAP) the softcap on every value.
+template <bool CAP>
+__device__ __forceinline__ void unpack8c(const uint4 &v, float (&z)[8], float cap_k, float cap_c) {
+  unpack_bf16x8(v, z);
+  if (CAP) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) z[j] = softcap_f(z[j], cap_k, cap_c);
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ float load_scalar(const void *row, int64_t v) {
   if (DT == DG_BF16) {
@@ -590,14 +600,14 @@ __device__ __forceinline__ int32_t segment_inner_draw(const void *row, int32_t V
 }
 
 // CAP: logits pass through the softcap (cap_k = 2 log2(e) / c, cap_c = c)
-// before any other use; capped calls take the per-group path.  SEG: the
-// candidate follows the segmented rule (no Gumbel screen, queue or shared
-// bound; one draw per segment of 32 indices, then the inner draw).
+// before any other use (on 16-byte-aligned bf16 rows in the ring, in
+// registers).  SEG: the candidate follows the segmented rule (no Gumbel
+// screen, queue or shared bound; one draw per segment of 32 indices, then the
+// inner draw).
 template <int DT, bool CAP, bool SEG>
-// The bf16 ring path runs 3 CTAs of 8 warps per SM (the ring and the queues
-// fill shared memory), at most 80 registers per thread; the other paths 4 CTAs
-// at 64.
-__global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
+// bf16 kernels run 3 CTAs of 8 warps per SM (the ring and the queues fill
+// shared memory), at most 80 registers per thread; fp32 ones 4 CTAs at 64.
+__global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
     vocab_pass_kernel(const void *__restrict__ logits, int64_t ld, int32_t V, int32_t C,
                       int64_t n_pos, int32_t chunk, int32_t n_chunks, uint64_t seed,
                       float cap_k, float cap_c,
@@ -674,7 +684,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
   Q.q = &s_queue[threadIdx.x >> 5][0];
   Q.head = 0;
   Q.count = 0;
-  if (!CAP && aligned && DT == DG_BF16) {
+  if (aligned && DT == DG_BF16) {
     const uint4 *vrow = reinterpret_cast<const uint4 *>(row) + g0;
     const int rounds = n_full / 128;
     // Per round each lane holds 4 groups (32 logits).  The round's maximum
@@ -694,7 +704,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
 #pragma unroll
       for (int u = 3; u >= 0; --u) {
         float z[8];
-        unpack_bf16x8(ld_stream(vrow + lane + u * 32), z);
+        unpack8c<CAP>(ld_stream(vrow + lane + u * 32), z, cap_k, cap_c);
 #pragma unroll
         for (int j = 7; j >= 0; --j)
           if (z[j] >= zb) {
@@ -741,7 +751,10 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
       uint4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) v[u] = cur[lane + u * 32];
-      const float rmax = round_max_bf16(v);
+      // the softcap is increasing, so the round's capped maximum is the cap
+      // of its raw maximum
+      float rmax = round_max_bf16(v);
+      if (CAP) rmax = softcap_f(rmax, cap_k, cap_c);
       if (rmax > L.zmax) am_round = rd;
       L.zmax = fmaxf(L.zmax, rmax);
       const float m2r = rmax * c;
@@ -752,8 +765,12 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float2 a = __ffma2_rn(
-              make_float2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u)), cc, mm);
+          float zl = __uint_as_float(w[k] << 16), zh = __uint_as_float(w[k] & 0xFFFF0000u);
+          if (CAP) {
+            zl = softcap_f(zl, cap_k, cap_c);
+            zh = softcap_f(zh, cap_k, cap_c);
+          }
+          const float2 a = __ffma2_rn(make_float2(zl, zh), cc, mm);
           const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
           if (k & 1) {
             L.S1 = __fadd2_rn(L.S1, e);
@@ -788,7 +805,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
           const uint32_t g = gq + 32u * u;
           const uint32_t h = fmix32(K.ka ^ g);
           float z[8];
-          unpack_bf16x8(cur[lane + u * 32], z);
+          unpack8c<CAP>(cur[lane + u * 32], z, cap_k, cap_c);
           coop_eval(h >= lim, z, g, h, c, wb, K, L, lane, Q);
         }
       }
@@ -803,7 +820,7 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
 #pragma unroll
       for (int u = 3; u >= 0; --u) {
         float z[8];
-        unpack_bf16x8(ld_stream(vrow + q + u * 32), z);
+        unpack8c<CAP>(ld_stream(vrow + q + u * 32), z, cap_k, cap_c);
 #pragma unroll
         for (int j = 7; j >= 0; --j)
           if (z[j] == L.zmax) best = (int32_t)((g0 + (uint32_t)(q + u * 32)) * kGroup + j);
@@ -817,14 +834,14 @@ __global__ void __launch_bounds__(kWarps * 32, (DT == DG_BF16 && !CAP) ? 3 : 4)
       bool pass = false;
       if constexpr (SEG) {
         if (q < n_full) {
-          unpack_bf16x8(ld_stream(vrow + q), z);
+          unpack8c<CAP>(ld_stream(vrow + q), z, cap_k, cap_c);
           const uint32_t g = g0 + (uint32_t)q;
           seg_add(L, segment_of_group(g), group8_seg(z, g, c, L), K);
         }
         continue;
       }
       if (q < n_full) {
-        unpack_bf16x8(ld_stream(vrow + q), z);
+        unpack8c<CAP>(ld_stream(vrow + q), z, cap_k, cap_c);
         pass = group8(z, g0 + (uint32_t)q, c, wb, K, L, h);
       }
       coop_eval(pass, z, g0 + (uint32_t)q, h, c, wb, K, L, lane, Q);
@@ -959,6 +976,12 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
       e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
     }
   }
@@ -967,7 +990,7 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const float cap_c = cap ? p.softcap : 0.f;
 #define DG_VOCAB_LAUNCH(DT, CAP, SEG)                                                         \
   vocab_pass_kernel<DT, CAP, SEG><<<(unsigned)blocks, kWarps * 32,                           \
-                                    (DT == DG_BF16 && !CAP) ? kRingBytes : 0, s>>>(          \
+                                    DT == DG_BF16 ? kRingBytes : 0, s>>>(                     \
       logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c, \
       st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status)
   const bool seg = p.sample_rule == DG_SAMPLE_SEGMENTED;
