@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
         fl |= q.flags;
         if (q.zmax > zmax || (q.zmax == zmax && q.am >= 0 && (pam < 0 || q.am < pam))) {
           if (q.zmax > zmax && S > 0.f) {  // the running maximum grows
-            const float d = zmax * c - q.zmax * c;
-            const float f = exp2f(d);
+            const float d = ceilf(zmax * c) - ceilf(q.zmax * c);
+            const float f = pow2_int(d);
             Tt = fmaf(d, S, Tt) * f;
             S *= f;
           }
@@ -143,8 +143,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
           pam = q.am;
         }
         if (q.s > 0.f) {
-          const float d = q.zmax * c - zmax * c;
-          const float f = exp2f(d);
+          const float d = ceilf(q.zmax * c) - ceilf(zmax * c);
+          const float f = pow2_int(d);
           S = fmaf(q.s, f, S);
           Tt = fmaf(fmaf(d, q.s, q.t), f, Tt);
         }
@@ -166,14 +166,14 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       if (nz != -INFINITY) {
         float ns = 0.f, nt2 = 0.f;
         if (S > 0.f) {
-          const float d = zmax * c - nz * c;
-          const float f = exp2f(d);
+          const float d = ceilf(zmax * c) - ceilf(nz * c);
+          const float f = pow2_int(d);
           ns = S * f;
           nt2 = fmaf(d, S, Tt) * f;
         }
         if (os > 0.f) {
-          const float d = oz * c - nz * c;
-          const float f = exp2f(d);
+          const float d = ceilf(oz * c) - ceilf(nz * c);
+          const float f = pow2_int(d);
           ns = fmaf(os, f, ns);
           nt2 = fmaf(fmaf(d, os, ot), f, nt2);
         }
@@ -193,15 +193,16 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       bool ok = !(fl & (kPartNaN | kPartPInf | kPartBadT)) && zmax != -INFINITY && pam >= 0 &&
                 pcand >= 0 && S > 0.f && isfinite(S) && isfinite(Tt);
       float Hf = NAN, m_out = NAN, s_out = NAN;
-      if (ok) {  // S >= 1 (the maximum contributes 2^0); fp32 keeps H within ~1e-6
+      if (ok) {  // S, Tt relative to ceil(zmax c): H does not depend on the reference
         Hf = 0.69314718f * (log2f(S) - __fdiv_rn(Tt, S));
         m_out = zmax / T;
-        s_out = S;
+        // s relative to the maximum itself: times 2^(ceil(zmax c) - zmax c)
+        s_out = S * exp2f(ceilf(zmax * c) - zmax * c);
       } else if (!(fl & kPartBadT)) {
         atomicOr(st.device_status, (uint32_t)DG_DEV_NONFINITE_LOGITS);
       }
       sH[i] = ok ? Hf : NAN;
-      sS[i] = ok ? S : NAN;
+      sS[i] = ok ? s_out : NAN;
       sAm[i] = ok ? pam : 0;
       sCand[i] = ok ? pcand : 0;
       st.m[base + i] = m_out;

@@ -93,6 +93,16 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// The softmax sums are kept relative to integer references (ceil of a
+// maximum of z c, c = log2(e) / T), so that moving a sum from one reference
+// to another multiplies it by 2^d with d a whole number: exact, where the
+// fast exp2 of a fraction would leave an error of one sign in every entropy
+// of a canvas.  pow2_int: 2^d for an integral d <= 0 (0 below 2^-126).
+__device__ __forceinline__ float pow2_int(float d) {
+  const int e = __float2int_rz(d);
+  return e < -126 ? 0.f : __int_as_float((127 + e) << 23);
+}
+
 // Logit softcap c tanh(z / c), from tanh x = 1 - 2 / (e^(2x) + 1):
 // c - 2c / (2^(z k) + 1) with k = 2 log2(e) / c.  +-inf map to +-c and NaN
 // stays NaN.  The absolute error is a few 1e-7 c (ex2.approx and the rounded
@@ -123,7 +133,7 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 
 // Per (position, vocabulary chunk) result of the vocabulary pass.
 //   zmax/am : largest stored logit of the chunk and its lowest index (-1 none)
-//   s, t    : sum 2^a and sum a 2^a, a = z*c - fl(zmax*c), c = log2(e)/T
+//   s, t    : sum 2^a and sum a 2^a, a = z*c - ceil(zmax*c), c = log2(e)/T
 //   b2/cand : best perturbed score (z*c - log2 E) and its lowest index
 //   flags   : kPartNaN / kPartPInf / kPartBadT
 struct alignas(16) Partial {

@@ -34,10 +34,11 @@ struct Keys {
 // than a few dozen terms: S/T collect one round of groups, BS/BT collect up
 // to 16 rounds, ts/tt the rest of the chunk.
 //
-// The sums are taken relative to a reference m2 (base 2), any value at or
-// below the running maximum of z c: with a = z c - m2, s = sum 2^a and
-// t = sum a 2^a give the same entropy log2 s - t/s for every choice of m2,
-// and the reference only keeps the terms in range.
+// The sums are taken relative to a reference m2 (base 2): an integer, so
+// that moving the sums to a new reference is exact (pow2_int).  With
+// a = z c - m2, s = sum 2^a and t = sum a 2^a give the same entropy
+// log2 s - t/s for every choice of m2; the reference only keeps the terms in
+// range.
 struct Lane {
   float zmax;   // running max of stored logits
   int32_t am;   // its lowest index (-1 until known)
@@ -95,8 +96,8 @@ __device__ __forceinline__ void rescale(Lane &L, float m2n) {
     L.m2 = m2n;
     return;
   }
-  const float d = L.m2 - m2n;
-  const float f = ex2_approx(d);
+  const float d = L.m2 - m2n;  // integral, <= 0
+  const float f = pow2_int(d);
   auto one = [&](float2 &S, float2 &T) {
     T.x = fmaf(d, S.x, T.x) * f;
     T.y = fmaf(d, S.y, T.y) * f;
@@ -207,7 +208,7 @@ __device__ __forceinline__ bool group8(const float (&z)[8], uint32_t g, float c,
 #pragma unroll
     for (int jj = 6; jj >= 0; --jj)
       if (z[jj] == vmax) j = jj;
-    const float m2n = vmax * c;
+    const float m2n = ceilf(vmax * c);
     rescale(L, m2n);
     L.zmax = vmax;
     L.am = (int32_t)(g * kGroup + j);
@@ -250,7 +251,7 @@ __device__ __forceinline__ float group8_seg(const float (&z)[8], uint32_t g, flo
 #pragma unroll
     for (int jj = 6; jj >= 0; --jj)
       if (z[jj] == vmax) j = jj;
-    const float m2n = vmax * c;
+    const float m2n = ceilf(vmax * c);
     rescale(L, m2n);
     L.zmax = vmax;
     L.am = (int32_t)(g * kGroup + j);
@@ -409,7 +410,7 @@ __device__ void group_careful(const float *z, int n, uint32_t g, float c, const 
   }
   if (vmax == -INFINITY) return;  // nothing finite in this group
   if (vmax > L.zmax) {
-    const float m2n = vmax * c;
+    const float m2n = ceilf(vmax * c);
     rescale(L, m2n);
     L.zmax = vmax;
     L.am = (int32_t)(g * kGroup + jm);
@@ -523,8 +524,8 @@ __device__ __forceinline__ void load_group(const void *row, bool aligned, int64_
 }
 
 // Merge the 32 lanes' records; every lane ends with the warp result, its sums
-// relative to fl(zmax c).  Each lane's sums come relative to its own
-// reference m2.
+// relative to ceil(zmax c).  Each lane's sums come relative to its own
+// (integral) reference m2.
 __device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32_t &am, float &s,
                                            float &t, float &b2, int32_t &cand) {
 #pragma unroll
@@ -536,20 +537,20 @@ __device__ __forceinline__ void warp_merge(float c, float m2, float &zmax, int32
     const float ot = __shfl_xor_sync(0xFFFFFFFFu, t, off);
     const float ob = __shfl_xor_sync(0xFFFFFFFFu, b2, off);
     const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, cand, off);
-    // softmax sums, relative to fl(zmax * c) on each side
+    // softmax sums, relative to ceil(zmax * c) on each side
     const float nz = fmaxf(zmax, oz);
     if (nz != -INFINITY) {
-      const float M2 = nz * c;
+      const float M2 = ceilf(nz * c);
       float ns = 0.f, nt = 0.f;
       if (s > 0.f) {
         const float d = m2 - M2;
-        const float f = ex2_approx(d);
+        const float f = pow2_int(d);
         ns += s * f;
         nt += fmaf(d, s, t) * f;
       }
       if (os > 0.f) {
         const float d = om2 - M2;
-        const float f = ex2_approx(d);
+        const float f = pow2_int(d);
         ns += os * f;
         nt += fmaf(d, os, ot) * f;
       }
@@ -757,7 +758,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
       if (CAP) rmax = softcap_f(rmax, cap_k, cap_c);
       if (rmax > L.zmax) am_round = rd;
       L.zmax = fmaxf(L.zmax, rmax);
-      const float m2r = rmax * c;
+      const float m2r = ceilf(rmax * c);
       if (m2r > L.m2 + kLazyRef) rescale(L, m2r);  // the first finite round sets it
       const float2 mm = make_float2(-L.m2, -L.m2);
 #pragma unroll
