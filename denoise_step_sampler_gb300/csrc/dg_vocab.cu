@@ -455,8 +455,11 @@ __device__ __forceinline__ uint32_t f2u_sat(float x) {
   return r;
 }
 // The sums' reference moves only when the maximum of z c passes it by more
-// than this (terms stay below 2^32, sums below 2^50).
-constexpr float kLazyRef = 32.f;
+// than this, so terms stay below 2^4.  A wider margin saved nothing: a term
+// far above the reference left the small terms added after it below half
+// a unit in the last place of their sum, where rounding drops them, and the
+// entropies came out low by up to a few 1e-7.
+constexpr float kLazyRef = 4.f;
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &v, float (&z)[8]) {
   z[0] = __uint_as_float(v.x << 16);
