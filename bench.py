@@ -431,11 +431,16 @@ def run_ours(args, rank, world, dev):
 
 
 def _selfcond_launches(p, d):
-    """Kernel launches of one dg_selfcond_embed call: the GEMM, plus the
-    split-K reduction when the library splits the vocabulary, which it does
-    exactly when the self-conditioning needs more workspace than the sampler
-    (its fp32 partial sums are [splits][rows][d])."""
+    """Kernel launches of one dg_selfcond_embed call: the GEMM; the split-K
+    reduction when the library splits the vocabulary (its fp32 partial sums,
+    [splits][rows][d], are the workspace beyond the sampler's and beyond a
+    softcapped feed's materialised p); and, for a softcapped feed, the kernel
+    that materialises p (bf16 rows of V rounded up to 8, 256-byte aligned)."""
     import denoise_step_sampler_gb300 as dg
+    rows = p.batch * p.canvas_len
+    if p.softcap > 0:
+        p_bytes = (rows * ((p.vocab + 7) // 8 * 8) * 2 + 255) // 256 * 256
+        return 2 + (1 if dg.dg_workspace_bytes(p, d) > p_bytes else 0)
     return 2 if dg.dg_workspace_bytes(p, d) > dg.dg_workspace_bytes(p, 0) else 1
 
 

@@ -45,10 +45,13 @@ struct SelfcondPlan {
   int32_t k_blocks;  // ceil(V / BK)
   int32_t kb_per_split;  // k-blocks per split (every split non-empty)
   int32_t n_sms;     // SMs the plan fills in whole waves
-  size_t ws_bytes;   // split-K partial sums (0 if splits == 1)
+  int64_t p_ld;      // softcapped feeds: elements per row of the materialised p (else 0)
+  size_t p_bytes;    // softcapped feeds: bytes of the materialised p (else 0)
+  size_t ws_bytes;   // p (capped feeds) + split-K partial sums (splits > 1)
 };
-// The split count depends on the sizes and on the number of SMs (n_sms).
-SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms);
+// The split count depends on the sizes and on the number of SMs (n_sms); a
+// softcapped feed (capped) also needs room for its materialised p.
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, bool capped);
 
 // SMs of the current device (cached per device); 152, the GB300's count, when
 // no device can be queried (host-only callers of the workspace query).

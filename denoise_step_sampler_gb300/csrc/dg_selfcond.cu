@@ -410,9 +410,10 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
 // column tile fastest and the row tile next, so the CTAs that read the same
 // logits tile (all column tiles of a row tile) and those that read the same E
 // tile (all row tiles of a column tile and split) run at the same time and
-// share both through L2.  CAP: the producers softcap the logits before the
-// rebuild.
-template <bool CAP>
+// share both through L2.  PRE: the A tiles are probabilities already (the
+// softcapped feed, materialised once by selfcond_pmat_kernel), so the
+// producers rebuild nothing and the MMA waits for the copies alone.
+template <bool PRE>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
                          const __grid_constant__ CUtensorMap tmap_z,
@@ -542,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&sh->full[s], (uint32_t)(i / NE) & 1u, sh, a.status,
                          where_code(1, 0, s, i)))
             break;
-          if (!mbar_wait(&sh->a_ready[sa], (uint32_t)(i / NA) & 1u, sh, a.status,
+          if (!mbar_wait(PRE ? &sh->a_full[sa] : &sh->a_ready[sa], (uint32_t)(i / NA) & 1u, sh, a.status,
                          where_code(1, 1, sa, i)))
             break;
           tc_fence_after();
@@ -582,7 +583,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t off[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) off[j] = a_off((t >> 3) + 64 * j, ch);
-      if (a.tma_a) {
+      if constexpr (PRE) {
+        // the tiles arrive as probabilities: nothing to rebuild
+      } else if (a.tma_a) {
         for (int i = 0; i < nkb; ++i) {
           const int s = i % NA;
           const uint32_t par = (uint32_t)(i / NA) & 1u;
@@ -599,12 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 4; ++j) {
               uint4 pv = make_uint4(0u, 0u, 0u, 0u);
               if ((okm >> j) & 1u) {
-                if constexpr (CAP) {
-                  const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                  pv = p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), 8, a.cap_k, a.cap_c);
-                } else {
-                  pv = p_from_bf16_full(v[j], cc2[j], nl2[j]);
-                }
+                pv = p_from_bf16_full(v[j], cc2[j], nl2[j]);
               }
               *reinterpret_cast<uint4 *>(tileA + off[j]) = pv;
             }
@@ -616,8 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
               uint4 pv = make_uint4(0u, 0u, 0u, 0u);
               if ((okm >> j) & 1u)
-                pv = CAP ? p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k, a.cap_c)
-                         : p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                pv = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               *reinterpret_cast<uint4 *>(tileA + off[j]) = pv;
             }
           }
@@ -656,13 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((okm >> j) & 1u) {
               if (a.dtype == DG_BF16) {
                 const uint32_t w[4] = {x[j].w[0], x[j].w[1], x[j].w[2], x[j].w[3]};
-                pv[j] = CAP ? p_from_bf16_cap(w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k,
-                                              a.cap_c)
-                            : p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                pv[j] = p_from_bf16(w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               } else {
-                pv[j] = CAP ? p_from_f32_cap(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid, a.cap_k,
-                                             a.cap_c)
-                            : p_from_f32(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
+                pv[j] = p_from_f32(x[j].w, lo2(cc2[j]), -lo2(nl2[j]), valid);
               }
             }
           }
@@ -744,6 +737,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The softcapped feed's probabilities, materialised once:
+//   p[q, v] = 2^(cap(z_{q,v}) c - l2_q)  (bf16; 0 for rows that do not feed)
+// so that the GEMM's tiles need no rebuild.  Rebuilt in the GEMM instead,
+// every column tile (11 at d = 2,816) would cap each logit again, three
+// transcendental operations per element each time.  One CTA per row; 16-byte
+// loads and stores along the row.
+__global__ void __launch_bounds__(256) selfcond_pmat_kernel(GemmArgs a, uint4 *p, int64_t p_ld) {
+  const int64_t q = blockIdx.x;
+  float c = 0.f, l2 = 0.f;
+  const bool ok = row_feeds(a, q, c, l2);
+  const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
+  const char *rowp = reinterpret_cast<const char *>(a.logits) + (size_t)q * (size_t)a.ld * esz;
+  uint4 *prow = p + (size_t)q * (size_t)(p_ld / 8);
+  const int64_t n8 = ((int64_t)a.V + 7) / 8;
+  for (int64_t g = threadIdx.x; g < n8; g += blockDim.x) {
+    uint4 out = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) {
+      const int64_t k = g * 8;
+      const int valid = (int)min((int64_t)8, (int64_t)a.V - k);
+      const Raw8 r = load_raw8(a, rowp, k);
+      if (a.dtype == DG_BF16) {
+        const uint32_t w[4] = {r.w[0], r.w[1], r.w[2], r.w[3]};
+        out = p_from_bf16_cap(w, c, l2, valid, a.cap_k, a.cap_c);
+      } else {
+        out = p_from_f32_cap(r.w, c, l2, valid, a.cap_k, a.cap_c);
+      }
+    }
+    prow[g] = out;
+  }
+}
+
 // out[q, :] = sum over splits of the partial sums, zeros for rows that do
 // not feed the next step.
 __global__ void selfcond_reduce_kernel(GemmArgs a) {
@@ -802,7 +826,7 @@ cudaError_t dg_selfcond_wait_record(uint32_t out[4]) {
   return cudaMemcpyFromSymbol(out, g_wait_record, sizeof(uint32_t) * 4);
 }
 
-SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms) {
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, bool capped) {
   SelfcondPlan pl;
   pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
   pl.n_tiles = (d + BN - 1) / BN;
@@ -827,12 +851,17 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms) {
   pl.kb_per_split = kbps;
   pl.splits = (pl.k_blocks + kbps - 1) / kbps;
   pl.n_sms = (int32_t)sms;
-  pl.ws_bytes = pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0;
+  // a softcapped feed materialises p first: rows of p_ld (V rounded up to 8)
+  // bf16, 256-byte aligned, ahead of the split-K partial sums
+  pl.p_ld = capped ? ((int64_t)V + 7) / 8 * 8 : 0;
+  pl.p_bytes = capped ? ((size_t)rows * (size_t)pl.p_ld * 2 + 255) / 256 * 256 : 0;
+  pl.ws_bytes = pl.p_bytes +
+                (pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0);
   return pl;
 }
 
 namespace {
-template <bool CAP>
+template <bool PRE>
 cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
                         const CUtensorMap &map_ep, const GemmArgs &a, int64_t grid,
                         cudaStream_t s) {
@@ -841,12 +870,12 @@ cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
   if (e != cudaSuccess) return e;
   static std::atomic<bool> attr_set[64];  // the shared-memory limit is raised once per device
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(selfcond_gemm_kernel<CAP>,
+    e = cudaFuncSetAttribute(selfcond_gemm_kernel<PRE>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  selfcond_gemm_kernel<CAP><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map_e, map_z, map_ep, a);
+  selfcond_gemm_kernel<PRE><<<(unsigned)grid, kThreads, kSmemBytes, s>>>(map_e, map_z, map_ep, a);
   return cudaSuccess;
 }
 
@@ -897,17 +926,21 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  const bool tma_a = p.logits_dtype == DG_BF16 &&
-                     (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
-                     (p.logits_ld * 2) % 16 == 0;
+  // Softcapped calls materialise p once in the workspace (plan.p_bytes,
+  // rows of plan.p_ld bf16), and the GEMM's A tiles come from there.
+  const bool pre = plan.p_bytes > 0;
+  const bool tma_a = pre || (p.logits_dtype == DG_BF16 &&
+                             (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
+                             (p.logits_ld * 2) % 16 == 0);
   memset(&map_z, 0, sizeof(map_z));
   if (tma_a) {
     const cuuint64_t dims[2] = {(cuuint64_t)p.vocab, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)p.logits_ld * 2};
+    const cuuint64_t strides[1] = {(cuuint64_t)(pre ? plan.p_ld : p.logits_ld) * 2};
     const cuuint32_t box[2] = {(cuuint32_t)BK, 128u};  // 64 columns x 128 rows (half a tile)
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&map_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(logits), dims,
-            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    void *base = pre ? ws : const_cast<void *>(logits);
+    if (enc(&map_z, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -934,16 +967,22 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.s = st.s;
   a.out = out;
   a.out_dtype = out_dtype;
-  a.partial = reinterpret_cast<float *>(ws);
+  a.partial = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + plan.p_bytes);
   a.status = st.device_status;
   const bool cap = p.softcap > 0.f;
   a.cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
   a.cap_c = cap ? p.softcap : 0.f;
   a.scale = p.embed_scale > 0.f ? p.embed_scale : 1.0f;
 
+  cudaError_t e;
+  if (pre) {
+    selfcond_pmat_kernel<<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   const int64_t grid = (int64_t)plan.m_tiles * plan.n_tiles * plan.splits;
-  cudaError_t e = cap ? launch_gemm<true>(map_e, map_z, map_ep, a, grid, s)
-                      : launch_gemm<false>(map_e, map_z, map_ep, a, grid, s);
+  e = pre ? launch_gemm<true>(map_e, map_z, map_ep, a, grid, s)
+          : launch_gemm<false>(map_e, map_z, map_ep, a, grid, s);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -167,7 +167,10 @@ typedef struct {
  * calls are ordered on one stream).  Returns 0 if `p` is invalid.  Depends on
  * the sizes in `p`, on d and on the SM count of the current device (the
  * self-conditioning GEMM splits the vocabulary to fill the SMs in whole
- * waves); query it with the device current that the calls will run on. */
+ * waves); query it with the device current that the calls will run on.  With
+ * p->softcap > 0 and d > 0 it includes the softcapped feed's probabilities,
+ * B*C rows of V rounded up to 8 bf16 (about B*C*V*2 bytes: 1.07 GB for
+ * 8 x 256 positions at V = 262,144). */
 size_t dg_workspace_bytes(const dg_params *p, int32_t d);
 
 /* Stand-alone canvas initialisation (the prefill case) of the rows r with
@@ -207,7 +210,10 @@ int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st,
  * `E`: device bf16 [V][ld_E], 16-byte aligned, ld_E >= d, ld_E*2 % 16 == 0.
  * `d`: 16 <= d, d % 16 == 0.  `out`: device [B*C][d] of out_dtype (DG_F32 or
  * DG_BF16).  `ws`: at least dg_workspace_bytes(p, d) bytes.  Products run on
- * the tensor cores in bf16 with fp32 accumulation. */
+ * the tensor cores in bf16 with fp32 accumulation.  Two or three kernel
+ * launches: with p->softcap > 0 a first kernel writes the probabilities of
+ * the capped logits to `ws` once, and the GEMM reads them from there; the
+ * GEMM; a split-K reduction when the vocabulary is split. */
 int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st,
                       const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                       void *ws, size_t ws_bytes, cudaStream_t stream);
