@@ -738,33 +738,48 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // The softcapped feed's probabilities, materialised once:
-//   p[q, v] = 2^(cap(z_{q,v}) c - l2_q)  (bf16; 0 for rows that do not feed)
+//   p[q, v] = 2^(cap(z_{q,v}) c - l2_q)  (bf16)
 // so that the GEMM's tiles need no rebuild.  Rebuilt in the GEMM instead,
 // every column tile (11 at d = 2,816) would cap each logit again, three
-// transcendental operations per element each time.  One CTA per row; 16-byte
-// loads and stores along the row.
+// transcendental operations per element each time.  One CTA per row; each
+// thread keeps four 16-byte loads in flight.  Rows that do not feed are not
+// written: the GEMM's epilogue writes zeros for them whatever their A rows
+// hold (row q of the product depends on row q of p alone).
+template <int DT>
+__device__ __forceinline__ uint4 pmat8(const GemmArgs &a, const Raw8 &r, float c, float l2,
+                                       int valid) {
+  if constexpr (DT == DG_BF16) {
+    const uint32_t w[4] = {r.w[0], r.w[1], r.w[2], r.w[3]};
+    return p_from_bf16_cap(w, c, l2, valid, a.cap_k, a.cap_c);
+  } else {
+    return p_from_f32_cap(r.w, c, l2, valid, a.cap_k, a.cap_c);
+  }
+}
+template <int DT>
 __global__ void __launch_bounds__(256) selfcond_pmat_kernel(GemmArgs a, uint4 *p, int64_t p_ld) {
   const int64_t q = blockIdx.x;
   float c = 0.f, l2 = 0.f;
-  const bool ok = row_feeds(a, q, c, l2);
-  const size_t esz = (a.dtype == DG_BF16) ? 2 : 4;
+  if (!row_feeds(a, q, c, l2)) return;
+  constexpr size_t esz = DT == DG_BF16 ? 2 : 4;
   const char *rowp = reinterpret_cast<const char *>(a.logits) + (size_t)q * (size_t)a.ld * esz;
   uint4 *prow = p + (size_t)q * (size_t)(p_ld / 8);
   const int64_t n8 = ((int64_t)a.V + 7) / 8;
-  for (int64_t g = threadIdx.x; g < n8; g += blockDim.x) {
-    uint4 out = make_uint4(0u, 0u, 0u, 0u);
-    if (ok) {
-      const int64_t k = g * 8;
-      const int valid = (int)min((int64_t)8, (int64_t)a.V - k);
-      const Raw8 r = load_raw8(a, rowp, k);
-      if (a.dtype == DG_BF16) {
-        const uint32_t w[4] = {r.w[0], r.w[1], r.w[2], r.w[3]};
-        out = p_from_bf16_cap(w, c, l2, valid, a.cap_k, a.cap_c);
-      } else {
-        out = p_from_f32_cap(r.w, c, l2, valid, a.cap_k, a.cap_c);
-      }
+  constexpr int U = 4;
+  const int64_t step = blockDim.x;
+  int64_t g = threadIdx.x;
+  for (; g + (U - 1) * step < n8; g += U * step) {
+    Raw8 r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = load_raw8(a, rowp, (g + u * step) * 8);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t k = (g + u * step) * 8;
+      prow[g + u * step] = pmat8<DT>(a, r[u], c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
     }
-    prow[g] = out;
+  }
+  for (; g < n8; g += step) {
+    const int64_t k = g * 8;
+    prow[g] = pmat8<DT>(a, load_raw8(a, rowp, k), c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
   }
 }
 
@@ -976,7 +991,10 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
 
   cudaError_t e;
   if (pre) {
-    selfcond_pmat_kernel<<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
+    if (p.logits_dtype == DG_BF16)
+      selfcond_pmat_kernel<DG_BF16><<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
+    else
+      selfcond_pmat_kernel<DG_F32><<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
