@@ -142,3 +142,34 @@ def test_embed_scale_is_an_exact_product(V, d):
         outs.append(out)
     torch.cuda.synchronize()
     assert torch.equal(outs[1], outs[0] * torch.tensor(2.75, dtype=torch.float32))
+
+
+@pytest.mark.parametrize("splitk", [False, True], ids=["one-pass", "split-K"])
+def test_softcap_rows_that_do_not_feed_are_zero_whatever_the_workspace_holds(splitk):
+    # the materialised p of rows that do not feed is never written; the
+    # workspace is filled with NaN bytes first, and those rows must still come
+    # out as exact zeros while the feeding rows match the oracle
+    B, C = 4, 64
+    V, d = (60000, 256) if splitk else (500, 32)
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=4,
+                  entropy_budget=50.0, conf_threshold=-1.0, stable_k=1, step_cap=2,
+                  softcap=30.0, embed_scale=8.0)
+    st = make_state(p, [dg.DG_PHASE_DENOISE, dg.DG_PHASE_PREFILL, dg.DG_PHASE_IDLE,
+                        dg.DG_PHASE_DENOISE], temperatures=[0.9, 1, 1, 1])
+    st.step[3] = 1  # reaches the cap: converges, does not feed
+    logits = syn.boosted_logits(B * C, V, seed=1, device="cuda", boost_hi=24.0).reshape(-1)
+    E = syn.embedding(V, d, seed=6, device="cuda")
+    ws = torch.full((max(16, dg.dg_workspace_bytes(p, d)),), 0xFF, dtype=torch.uint8, device="cuda")
+    dg.dg_denoise_step(p, logits, st, ws)
+    ws.fill_(0xFF)
+    out = torch.full((B * C, d), float("nan"), dtype=torch.float32, device="cuda")
+    dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+    torch.cuda.synchronize()
+    assert int(st.device_status.item()) == 0
+    assert st.snapshot()["sc_valid"].tolist() == [1, 0, 0, 0]
+    got = out.view(B, C, d)
+    assert torch.count_nonzero(got[1:]).item() == 0
+    zh = logits.view(B, C, V)[0].float().cpu().numpy().astype(np.float64)
+    ref = osc.selfcond_rows(zh, float(np.float32(0.9)), E.float().cpu().numpy().astype(np.float64),
+                            cap=30.0, scale=8.0)
+    selfcond_check(got[0].cpu().numpy(), ref)
