@@ -138,6 +138,24 @@ __device__ __forceinline__ void seg_close(Lane &L, const Keys &K) {
   L.pk = -1;
   L.pseg = 0.f;
 }
+// Score segment k of total mass `mass` (relative to L.m2) at once, when no
+// segment is pending: the same as seg_add(k, mass) then seg_close.  The
+// segment beats the best score b2 only if its draw E is below
+// tau = mass 2^(m2 - b2), and E >= W = 1 - U = (~h + 1/2) 2^-32 (as
+// -ln U >= 1 - U), so a segment whose W is above tau (with a 0.1 % margin
+// for rounding) is skipped without its logarithms.
+__device__ __forceinline__ void seg_score(Lane &L, int32_t k, float mass, const Keys &K) {
+  const uint32_t h = fmix32(K.ks ^ (uint32_t)k);
+  const float tau = mass * ex2_approx(L.m2 - L.b2);
+  if ((float)(~h) * 2.3283064365386963e-10f <= tau * 1.001f && mass > 0.f) {
+    const float E = exp1_draw_uniform(h);
+    const float sc = L.m2 + (__log2f(mass) - __log2f(E));
+    if (sc > L.b2 || (sc == L.b2 && k < L.cand)) {
+      L.b2 = sc;
+      L.cand = k;
+    }
+  }
+}
 // Add the mass (relative to L.m2) of some indices of segment k.
 __device__ __forceinline__ void seg_add(Lane &L, int32_t k, float mass, const Keys &K) {
   if (k != L.pk) {
@@ -157,6 +175,17 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
                    (uint32_t)__cvta_generic_to_shared(dst)),
                "l"(src)
                : "memory");
+}
+__device__ __forceinline__ void cp_async16s(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
@@ -729,40 +758,48 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
       for (int off = 16; off > 0; off >>= 1) wb = fmaxf(wb, __shfl_xor_sync(0xFFFFFFFFu, wb, off));
       share_bound(slot, wb, lane);
     }
-    uint4 *ring = s_ring + (size_t)(threadIdx.x >> 5) * (kStages * 128);
+    // this lane's slots of the warp's ring (a shared-memory address), and
+    // the next round to issue
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(
+        s_ring + (size_t)(threadIdx.x >> 5) * (kStages * 128) + lane);
+    const uint4 *nxt = vrow + lane;
 #pragma unroll
     for (int r = 0; r < kStages - 1; ++r) {
       if (r < rounds) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          cp_async16(ring + r * 128 + lane + u * 32, vrow + r * 128 + lane + u * 32);
+        for (int u = 0; u < 4; ++u) cp_async16s(ring + (r * 128 + u * 32) * 16, nxt + u * 32);
       }
+      nxt += 128;
       cp_async_commit();
     }
-    for (int rd = 0; rd < rounds; ++rd) {
-      const int q = rd * 128 + lane;
-      {
-        const int r = rd + kStages - 1;
-        if (r < rounds) {
+    // Round rd is read from stage sc while round rd + 2 is issued into stage
+    // si; both counters rotate, so no round computes a modulo or a 64-bit
+    // source address.
+    const uint32_t sb0 = (uint32_t)(v0 / 1024);  // superblock of round 0
+    int sc = 0, si = kStages - 1;
+    for (int rd = 0; rd < rounds;
+         ++rd, sc = (sc == kStages - 1) ? 0 : sc + 1, si = (si == kStages - 1) ? 0 : si + 1) {
+      if (rd + kStages - 1 < rounds) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            cp_async16(ring + (r % kStages) * 128 + lane + u * 32, vrow + r * 128 + lane + u * 32);
-        }
-        cp_async_commit();
+        for (int u = 0; u < 4; ++u) cp_async16s(ring + (si * 128 + u * 32) * 16, nxt + u * 32);
       }
+      nxt += 128;
+      cp_async_commit();
       cp_async_wait<kStages - 1>();
-      const uint4 *cur = ring + (rd % kStages) * 128;
+      const uint32_t cur = ring + sc * 128 * 16;
       uint4 v[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) v[u] = cur[lane + u * 32];
+      for (int u = 0; u < 4; ++u) v[u] = ld_shared16(cur + u * 32 * 16);
       // the softcap is increasing, so the round's capped maximum is the cap
       // of its raw maximum
       float rmax = round_max_bf16(v);
       if (CAP) rmax = softcap_f(rmax, cap_k, cap_c);
       if (rmax > L.zmax) am_round = rd;
       L.zmax = fmaxf(L.zmax, rmax);
-      const float m2r = ceilf(rmax * c);
-      if (m2r > L.m2 + kLazyRef) rescale(L, m2r);  // the first finite round sets it
+      // L.m2 + kLazyRef is a whole number, so comparing rmax c with it
+      // decides the same as comparing its ceiling
+      const float xr = rmax * c;
+      if (xr > L.m2 + kLazyRef) rescale(L, ceilf(xr));  // the first finite round sets it
       const float2 mm = make_float2(-L.m2, -L.m2);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -789,16 +826,18 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
         // the round is lane's whole segment of superblock (v0 / 1024 + rd):
         // its mass is the round's sums, scored at once
         const float2 es = __fadd2_rn(L.S0, L.S1);
-        seg_add(L, (int32_t)(32u * (uint32_t)(v0 / 1024 + rd) + (uint32_t)lane), es.x + es.y, K);
-        seg_close(L, K);
-        if ((rd & 15) == 15) fold_block(L); else fold_round(L);
+        seg_score(L, (int32_t)(32u * (uint32_t)(sb0 + rd) + (uint32_t)lane), es.x + es.y, K);
+        L.BS = __fadd2_rn(L.BS, es);
+        L.BT = __fadd2_rn(L.BT, __fadd2_rn(L.T0, L.T1));
+        L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
+        if ((rd & 15) == 15) fold_block(L);
         continue;
       }
       // Gumbel screen: group g can hold a score >= wb only if its W_g
       // (= (~h + 1/2) 2^-32) <= 8 2^(vmax c - wb); with the round maximum for
       // vmax and a 0.1 % margin that is ~h <= 2^(rmax c - wb + 35.00144).
       const uint32_t lim = ~f2u_sat(ex2_approx(fmaf(rmax, c, -wb) + 35.0014415f));
-      const uint32_t gq = g0 + (uint32_t)q;
+      const uint32_t gq = g0 + (uint32_t)(rd * 128 + lane);
       bool any = false;
 #pragma unroll
       for (int u = 0; u < 4; ++u) any |= fmix32(K.ka ^ (gq + 32u * u)) >= lim;
@@ -809,7 +848,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
           const uint32_t g = gq + 32u * u;
           const uint32_t h = fmix32(K.ka ^ g);
           float z[8];
-          unpack8c<CAP>(cur[lane + u * 32], z, cap_k, cap_c);
+          unpack8c<CAP>(ld_shared16(cur + u * 32 * 16), z, cap_k, cap_c);
           coop_eval(h >= lim, z, g, h, c, wb, K, L, lane, Q);
         }
       }
