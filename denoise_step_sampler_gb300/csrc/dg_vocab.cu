@@ -72,11 +72,15 @@ __device__ __forceinline__ void fold_round(Lane &L) {
   L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
 }
 // Block sums into the chunk totals.
-__device__ __forceinline__ void fold_block(Lane &L) {
-  fold_round(L);
+// Block sums into the chunk totals.
+__device__ __forceinline__ void fold_block_sums(Lane &L) {
   L.ts += L.BS.x + L.BS.y;
   L.tt += L.BT.x + L.BT.y;
   L.BS = L.BT = make_float2(0.f, 0.f);
+}
+__device__ __forceinline__ void fold_block(Lane &L) {
+  fold_round(L);
+  fold_block_sums(L);
 }
 
 __device__ __forceinline__ void sums(Lane &L, float &s, float &t) {
@@ -775,7 +779,9 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
     // Round rd is read from stage sc while round rd + 2 is issued into stage
     // si; both counters rotate, so no round computes a modulo or a 64-bit
     // source address.
-    const uint32_t sb0 = (uint32_t)(v0 / 1024);  // superblock of round 0
+    // the segment of round 0 (superblock v0 / 1024): each round is one
+    // segment per lane, 32 segments on
+    int32_t segk = (int32_t)(32u * (uint32_t)(v0 / 1024) + (uint32_t)lane);
     int sc = 0, si = kStages - 1;
     for (int rd = 0; rd < rounds;
          ++rd, sc = (sc == kStages - 1) ? 0 : sc + 1, si = (si == kStages - 1) ? 0 : si + 1) {
@@ -813,7 +819,17 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
           }
           const float2 a = __ffma2_rn(make_float2(zl, zh), cc, mm);
           const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-          if (k & 1) {
+          if (SEG && u == 0 && k < 2) {
+            // the segmented rule's round sums start from the round's first
+            // pairs instead of from zeros (the same values: 0 + e = e)
+            if (k & 1) {
+              L.S1 = e;
+              L.T1 = __fmul2_rn(a, e);
+            } else {
+              L.S0 = e;
+              L.T0 = __fmul2_rn(a, e);
+            }
+          } else if (k & 1) {
             L.S1 = __fadd2_rn(L.S1, e);
             L.T1 = __ffma2_rn(a, e, L.T1);
           } else {
@@ -826,11 +842,11 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
         // the round is lane's whole segment of superblock (v0 / 1024 + rd):
         // its mass is the round's sums, scored at once
         const float2 es = __fadd2_rn(L.S0, L.S1);
-        seg_score(L, (int32_t)(32u * (uint32_t)(sb0 + rd) + (uint32_t)lane), es.x + es.y, K);
+        seg_score(L, segk, es.x + es.y, K);
+        segk += 32;
         L.BS = __fadd2_rn(L.BS, es);
         L.BT = __fadd2_rn(L.BT, __fadd2_rn(L.T0, L.T1));
-        L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
-        if ((rd & 15) == 15) fold_block(L);
+        if ((rd & 15) == 15) fold_block_sums(L);
         continue;
       }
       // Gumbel screen: group g can hold a score >= wb only if its W_g
@@ -855,6 +871,9 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
     }
+    // the segmented rule's round sums hold the last round's values (already
+    // folded); the paths after the ring add to them from zero
+    if constexpr (SEG) L.S0 = L.S1 = L.T0 = L.T1 = make_float2(0.f, 0.f);
     cp_async_wait<0>();
     if (am_round >= 0) {
       // lowest index holding the lane's maximum, in the round that set it
