@@ -4,11 +4,13 @@ times:
 
 * 1 canvas x 256, V = 50257, fp32 logits (unaligned rows), d = 512: every
   position and every self-conditioning row;
-* 8 canvases x 256, V = 262144, bf16, d = 2816: one full canvas (acceptance
-  and re-noise included), 64 random positions, 8 self-conditioning rows;
+* 8 canvases x 256, V = 262144, bf16, d = 2816, both sampling rules: one
+  full canvas (acceptance and re-noise included), 64 random positions, two
+  self-conditioning rows from every 256-row tile of the GEMM;
 * the same with the logit softcap (c = 30) and the sqrt(d) embedding scale;
-* 128 canvases x 256 (17 GB of logits): one full canvas, 64 random positions,
-  4 self-conditioning rows;
+* 16, 32 and 64 canvases (the sweep sizes) and 128 canvases x 256 (17 GB of
+  logits, both sampling rules): one full canvas, 64 random positions, two
+  self-conditioning rows from every 256-row tile of the GEMM;
 * the mixed-phase loop (32 requests: 8 prefill, 20 denoise, 4 commit) at
   V = 262144: the first two steps compared for three requests from the GPU's
   prior state, then run until every request has committed, checking the phase
@@ -143,9 +145,12 @@ def test_eight_canvases_V262144_bf16_sampled(rule):
               sample_rule=rule)
 
 
-def test_32_canvases_V262144_bf16_sampled():
-    # another split plan of the GEMM and 4 vocabulary chunks per position
-    _one_step(32, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, 0xD1FF0006, 64, 2,
+@pytest.mark.parametrize("B,seed", [(16, 0xD1FF0007), (32, 0xD1FF0006), (64, 0xD1FF0008)],
+                         ids=["16", "32", "64"])
+def test_sweep_canvases_V262144_bf16_sampled(B, seed):
+    # the sweep sizes: other split plans of the GEMM (on 152 SMs: 6 splits at
+    # 16 canvases, 3 from 32 on) and 4 or 2 vocabulary chunks per position
+    _one_step(B, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, seed, 64, 2,
               sample_rule=dg.DG_SAMPLE_SEGMENTED)
 
 
@@ -155,8 +160,12 @@ def test_eight_canvases_softcap_and_embed_scale_sampled():
               softcap=30.0, embed_scale=float(np.sqrt(2816.0)))
 
 
-def test_128_canvases_V262144_bf16_sampled():
-    _one_step(128, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, 0xD1FF0004, 64, 2)
+@pytest.mark.parametrize("rule", [dg.DG_SAMPLE_SEGMENTED, dg.DG_SAMPLE_GROUPED],
+                         ids=["segmented", "grouped"])
+def test_128_canvases_V262144_bf16_sampled(rule):
+    # the benchmark's default workload and rule, and the grouped rule
+    _one_step(128, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, 0xD1FF0004, 64, 2,
+              sample_rule=rule)
 
 
 def test_mixed_phase_loop_full_vocab():
