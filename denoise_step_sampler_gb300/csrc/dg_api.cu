@@ -44,24 +44,35 @@ size_t denoise_ws_bytes(const dg_params *p) {
   return round_up((size_t)n_pos * (size_t)vc.n_chunks * sizeof(Partial), 256);
 }
 
-int32_t device_sm_count() {
+namespace {
+// An attribute of the current device, cached per device; `fallback` when no
+// device can be queried (host-only callers of the workspace query).
+int64_t device_attr(cudaDeviceAttr attr, std::atomic<int64_t> (&cache)[64], int64_t fallback) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
-    return 152;
+    return fallback;
   }
-  static std::atomic<int32_t> cache[64];  // 0 = not yet queried
   if (dev >= 0 && dev < 64) {
-    const int32_t c = cache[dev].load(std::memory_order_relaxed);
+    const int64_t c = cache[dev].load(std::memory_order_relaxed);
     if (c > 0) return c;
   }
   int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+  if (cudaDeviceGetAttribute(&n, attr, dev) != cudaSuccess || n <= 0) {
     cudaGetLastError();
-    return 152;
+    return fallback;
   }
   if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
   return n;
+}
+std::atomic<int64_t> g_sm_cache[64], g_l2_cache[64];  // 0 = not yet queried
+}  // namespace
+
+int32_t device_sm_count() {
+  return (int32_t)device_attr(cudaDevAttrMultiProcessorCount, g_sm_cache, 152);
+}
+int64_t device_l2_bytes() {
+  return device_attr(cudaDevAttrL2CacheSize, g_l2_cache, kGB300L2Bytes);
 }
 
 // The device must be an sm_103 part (GB300); checked once per device.
@@ -123,7 +134,7 @@ size_t dg_workspace_bytes(const dg_params *p, int32_t d) {
   size_t ws = denoise_ws_bytes(p);
   if (d > 0) {
     const SelfcondPlan pl = selfcond_plan((int64_t)p->batch * p->canvas_len, p->vocab, d,
-                                          device_sm_count(), p->softcap > 0.f);
+                                          device_sm_count(), device_l2_bytes(), p->softcap > 0.f);
     if (pl.ws_bytes > ws) ws = pl.ws_bytes;
   }
   return ws;
@@ -201,7 +212,8 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
   const size_t esz = p->logits_dtype == DG_BF16 ? 2 : 4;
   if (!aligned(logits, esz) || !aligned(E, 16) || !aligned(out, 16)) return DG_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)p->batch * p->canvas_len;
-  const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d, device_sm_count(), p->softcap > 0.f);
+  const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d, device_sm_count(), device_l2_bytes(),
+                                        p->softcap > 0.f);
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned(ws, 16)))
     return DG_ERR_WORKSPACE;
   const int dv = device_ok();

@@ -49,13 +49,19 @@ struct SelfcondPlan {
   size_t p_bytes;    // softcapped feeds: bytes of the materialised p (else 0)
   size_t ws_bytes;   // p (capped feeds) + split-K partial sums (splits > 1)
 };
-// The split count depends on the sizes and on the number of SMs (n_sms); a
-// softcapped feed (capped) also needs room for its materialised p.
-SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, bool capped);
+// The split count depends on the sizes, on the number of SMs (n_sms) and, for
+// more than 64 row tiles, on the L2 size (l2_bytes); a softcapped feed
+// (capped) also needs room for its materialised p.
+SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, int64_t l2_bytes,
+                           bool capped);
 
 // SMs of the current device (cached per device); 152, the GB300's count, when
 // no device can be queried (host-only callers of the workspace query).
 int32_t device_sm_count();
+// L2 bytes of the current device (cached per device); the GB300's when no
+// device can be queried.
+constexpr int64_t kGB300L2Bytes = 135528448;
+int64_t device_l2_bytes();
 cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                             void *ws, const SelfcondPlan &plan, cudaStream_t s);

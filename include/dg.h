@@ -165,9 +165,11 @@ typedef struct {
 /* Bytes of caller workspace needed by dg_denoise_step and, if d > 0, by
  * dg_selfcond_embed with embedding width d (one buffer serves both, as the
  * calls are ordered on one stream).  Returns 0 if `p` is invalid.  Depends on
- * the sizes in `p`, on d and on the SM count of the current device (the
- * self-conditioning GEMM splits the vocabulary to fill the SMs in whole
- * waves); query it with the device current that the calls will run on.  With
+ * the sizes in `p`, on d and on the SM count and L2 size of the current
+ * device (the self-conditioning GEMM splits the vocabulary to fill the SMs in
+ * whole waves and, for more than 64 row tiles of 256 positions, until one
+ * split's slice of E fits in L2); query it with the device current that the
+ * calls will run on.  With
  * p->softcap > 0 and d > 0 it includes the softcapped feed's probabilities,
  * B*C rows of V rounded up to 8 bf16 (about B*C*V*2 bytes: 1.07 GB for
  * 8 x 256 positions at V = 262,144). */
