@@ -7,7 +7,8 @@ times:
 * 8 canvases x 256, V = 262144, bf16, d = 2816, both sampling rules: one
   full canvas (acceptance and re-noise included), 64 random positions, two
   self-conditioning rows from every 256-row tile of the GEMM;
-* the same with the logit softcap (c = 30) and the sqrt(d) embedding scale;
+* the same with the logit softcap (c = 30) and the sqrt(d) embedding scale,
+  at 8 and at 128 canvases;
 * 16, 32 and 64 canvases (the sweep sizes) and 128 canvases x 256 (17 GB of
   logits, both sampling rules): one full canvas, 64 random positions, two
   self-conditioning rows from every 256-row tile of the GEMM;
@@ -158,6 +159,13 @@ def test_eight_canvases_softcap_and_embed_scale_sampled():
     # the softcapped path (c = 30) with the sqrt(d) embedding scale on the feed
     _one_step(8, 256, 262144, dg.DG_BF16, 0.8, 96.0, 2816, 16.0, 0xD1FF0005, 64, 2,
               softcap=30.0, embed_scale=float(np.sqrt(2816.0)))
+
+
+def test_128_canvases_softcap_and_embed_scale_sampled():
+    # the softcapped feed at the largest workload: a 17 GB materialised p in
+    # the workspace and the GEMM's L2-fitted split count (11 on a GB300)
+    _one_step(128, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, 0xD1FF0009, 64, 2,
+              softcap=30.0, embed_scale=float(np.sqrt(2816.0)), sample_rule=dg.DG_SAMPLE_SEGMENTED)
 
 
 @pytest.mark.parametrize("rule", [dg.DG_SAMPLE_SEGMENTED, dg.DG_SAMPLE_GROUPED],
