@@ -441,11 +441,14 @@ def _selfcond_launches(p, d):
     """Kernel launches of one dg_selfcond_embed call: the GEMM; the split-K
     reduction when the library splits the vocabulary (its fp32 partial sums,
     [splits][rows][d], are the workspace beyond the sampler's and beyond a
-    softcapped feed's materialised p); and, for a softcapped feed, the kernel
-    that materialises p (bf16 rows of V rounded up to 8, 256-byte aligned)."""
+    materialised p); and the kernel that materialises p (bf16 rows of V
+    rounded up to 8, 256-byte aligned) for a softcapped feed or for logits the
+    GEMM cannot copy by TMA (fp32, or bf16 rows whose stride is not a multiple
+    of 16 bytes)."""
     import denoise_step_sampler_gb300 as dg
     rows = p.batch * p.canvas_len
-    if p.softcap > 0:
+    ld = p.logits_ld or p.vocab
+    if p.softcap > 0 or p.logits_dtype != dg.DG_BF16 or (ld * 2) % 16:
         p_bytes = (rows * ((p.vocab + 7) // 8 * 8) * 2 + 255) // 256 * 256
         return 2 + (1 if dg.dg_workspace_bytes(p, d) > p_bytes else 0)
     return 2 if dg.dg_workspace_bytes(p, d) > dg.dg_workspace_bytes(p, 0) else 1

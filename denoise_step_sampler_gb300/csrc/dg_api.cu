@@ -134,7 +134,8 @@ size_t dg_workspace_bytes(const dg_params *p, int32_t d) {
   size_t ws = denoise_ws_bytes(p);
   if (d > 0) {
     const SelfcondPlan pl = selfcond_plan((int64_t)p->batch * p->canvas_len, p->vocab, d,
-                                          device_sm_count(), device_l2_bytes(), p->softcap > 0.f);
+                                          device_sm_count(), device_l2_bytes(),
+                                          selfcond_materialises(*p));
     if (pl.ws_bytes > ws) ws = pl.ws_bytes;
   }
   return ws;
@@ -213,7 +214,7 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
   if (!aligned(logits, esz) || !aligned(E, 16) || !aligned(out, 16)) return DG_ERR_INVALID_ARG;
   const int64_t rows = (int64_t)p->batch * p->canvas_len;
   const SelfcondPlan pl = selfcond_plan(rows, p->vocab, d, device_sm_count(), device_l2_bytes(),
-                                        p->softcap > 0.f);
+                                        selfcond_materialises(*p));
   if (pl.ws_bytes > 0 && (!ws || ws_bytes < pl.ws_bytes || !aligned(ws, 16)))
     return DG_ERR_WORKSPACE;
   const int dv = device_ok();

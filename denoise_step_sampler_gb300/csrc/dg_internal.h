@@ -45,15 +45,21 @@ struct SelfcondPlan {
   int32_t k_blocks;  // ceil(V / BK)
   int32_t kb_per_split;  // k-blocks per split (every split non-empty)
   int32_t n_sms;     // SMs the plan fills in whole waves
-  int64_t p_ld;      // softcapped feeds: elements per row of the materialised p (else 0)
-  size_t p_bytes;    // softcapped feeds: bytes of the materialised p (else 0)
-  size_t ws_bytes;   // p (capped feeds) + split-K partial sums (splits > 1)
+  int64_t p_ld;      // materialised p: elements per row (else 0)
+  size_t p_bytes;    // materialised p: bytes (else 0)
+  size_t ws_bytes;   // materialised p + split-K partial sums (splits > 1)
 };
 // The split count depends on the sizes, on the number of SMs (n_sms) and, for
-// more than 64 row tiles, on the L2 size (l2_bytes); a softcapped feed
-// (capped) also needs room for its materialised p.
+// more than 64 row tiles, on the L2 size (l2_bytes); with `materialise` (see
+// selfcond_materialises) the plan also holds the materialised p.
 SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, int64_t l2_bytes,
-                           bool capped);
+                           bool materialise);
+// Whether the self-conditioning call materialises p before the GEMM: a
+// softcapped feed, or logits the GEMM cannot copy by TMA (fp32, or bf16 rows
+// whose stride is not a multiple of 16 bytes).
+inline bool selfcond_materialises(const dg_params &p) {
+  return p.softcap > 0.f || p.logits_dtype != DG_BF16 || (p.logits_ld * 2) % 16 != 0;
+}
 
 // SMs of the current device (cached per device); 152, the GB300's count, when
 // no device can be queried (host-only callers of the workspace query).

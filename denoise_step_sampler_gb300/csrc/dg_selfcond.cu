@@ -410,9 +410,9 @@ __device__ __forceinline__ uint32_t a_off(int r, int ch) {
 // column tile fastest and the row tile next, so the CTAs that read the same
 // logits tile (all column tiles of a row tile) and those that read the same E
 // tile (all row tiles of a column tile and split) run at the same time and
-// share both through L2.  PRE: the A tiles are probabilities already (the
-// softcapped feed, materialised once by selfcond_pmat_kernel), so the
-// producers rebuild nothing and the MMA waits for the copies alone.
+// share both through L2.  PRE: the A tiles are probabilities already
+// (materialised once by selfcond_pmat_kernel), so the producers rebuild
+// nothing and the MMA waits for the copies alone.
 template <bool PRE>
 __global__ void __launch_bounds__(kThreads, 1)
     selfcond_gemm_kernel(const __grid_constant__ CUtensorMap tmap_e,
@@ -737,25 +737,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// The softcapped feed's probabilities, materialised once:
-//   p[q, v] = 2^(cap(z_{q,v}) c - l2_q)  (bf16)
-// so that the GEMM's tiles need no rebuild.  Rebuilt in the GEMM instead,
-// every column tile (11 at d = 2,816) would cap each logit again, three
-// transcendental operations per element each time.  One CTA per row; each
+// The feed's probabilities, materialised once:
+//   p[q, v] = 2^(z'_{q,v} c - l2_q)  (bf16), z' = cap(z) for a softcapped feed
+// so that the GEMM's tiles need no rebuild.  Used where the rebuild would be
+// slow: softcapped feeds (rebuilt in the GEMM, every column tile, 11 at
+// d = 2,816, would cap each logit again, three transcendental operations per
+// element each time), and logits the GEMM cannot copy by TMA (fp32, or bf16
+// rows whose stride is not a multiple of 16 bytes), which its producers would
+// otherwise load one stage ahead with plain loads.  One CTA per row; each
 // thread keeps four 16-byte loads in flight.  Rows that do not feed are not
 // written: the GEMM's epilogue writes zeros for them whatever their A rows
 // hold (row q of the product depends on row q of p alone).
-template <int DT>
+template <int DT, bool CAP>
 __device__ __forceinline__ uint4 pmat8(const GemmArgs &a, const Raw8 &r, float c, float l2,
                                        int valid) {
   if constexpr (DT == DG_BF16) {
     const uint32_t w[4] = {r.w[0], r.w[1], r.w[2], r.w[3]};
-    return p_from_bf16_cap(w, c, l2, valid, a.cap_k, a.cap_c);
+    if constexpr (CAP) return p_from_bf16_cap(w, c, l2, valid, a.cap_k, a.cap_c);
+    else return p_from_bf16(w, c, l2, valid);
   } else {
-    return p_from_f32_cap(r.w, c, l2, valid, a.cap_k, a.cap_c);
+    if constexpr (CAP) return p_from_f32_cap(r.w, c, l2, valid, a.cap_k, a.cap_c);
+    else return p_from_f32(r.w, c, l2, valid);
   }
 }
-template <int DT>
+template <int DT, bool CAP>
 __global__ void __launch_bounds__(256) selfcond_pmat_kernel(GemmArgs a, uint4 *p, int64_t p_ld) {
   const int64_t q = blockIdx.x;
   float c = 0.f, l2 = 0.f;
@@ -774,12 +779,12 @@ __global__ void __launch_bounds__(256) selfcond_pmat_kernel(GemmArgs a, uint4 *p
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t k = (g + u * step) * 8;
-      prow[g + u * step] = pmat8<DT>(a, r[u], c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
+      prow[g + u * step] = pmat8<DT, CAP>(a, r[u], c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
     }
   }
   for (; g < n8; g += step) {
     const int64_t k = g * 8;
-    prow[g] = pmat8<DT>(a, load_raw8(a, rowp, k), c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
+    prow[g] = pmat8<DT, CAP>(a, load_raw8(a, rowp, k), c, l2, (int)min((int64_t)8, (int64_t)a.V - k));
   }
 }
 
@@ -842,7 +847,7 @@ cudaError_t dg_selfcond_wait_record(uint32_t out[4]) {
 }
 
 SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, int64_t l2_bytes,
-                           bool capped) {
+                           bool materialise) {
   SelfcondPlan pl;
   pl.m_tiles = (int32_t)((rows + BM - 1) / BM);
   pl.n_tiles = (d + BN - 1) / BN;
@@ -877,10 +882,11 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, in
   pl.kb_per_split = kbps;
   pl.splits = (pl.k_blocks + kbps - 1) / kbps;
   pl.n_sms = (int32_t)sms;
-  // a softcapped feed materialises p first: rows of p_ld (V rounded up to 8)
-  // bf16, 256-byte aligned, ahead of the split-K partial sums
-  pl.p_ld = capped ? ((int64_t)V + 7) / 8 * 8 : 0;
-  pl.p_bytes = capped ? ((size_t)rows * (size_t)pl.p_ld * 2 + 255) / 256 * 256 : 0;
+  // a materialised p (softcapped feeds, logits the GEMM cannot copy by TMA):
+  // rows of p_ld (V rounded up to 8) bf16, 256-byte aligned, ahead of the
+  // split-K partial sums
+  pl.p_ld = materialise ? ((int64_t)V + 7) / 8 * 8 : 0;
+  pl.p_bytes = materialise ? ((size_t)rows * (size_t)pl.p_ld * 2 + 255) / 256 * 256 : 0;
   pl.ws_bytes = pl.p_bytes +
                 (pl.splits > 1 ? (size_t)pl.splits * (size_t)rows * (size_t)d * sizeof(float) : 0);
   return pl;
@@ -952,8 +958,10 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // Softcapped calls materialise p once in the workspace (plan.p_bytes,
-  // rows of plan.p_ld bf16), and the GEMM's A tiles come from there.
+  // Softcapped calls, and logits that the GEMM cannot copy by TMA (fp32, or
+  // bf16 rows whose stride is not a multiple of 16 bytes), materialise p once
+  // in the workspace (plan.p_bytes, rows of plan.p_ld bf16), and the GEMM's
+  // A tiles come from there.
   const bool pre = plan.p_bytes > 0;
   const bool tma_a = pre || (p.logits_dtype == DG_BF16 &&
                              (reinterpret_cast<uintptr_t>(logits) % 16) == 0 &&
@@ -1002,10 +1010,14 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
 
   cudaError_t e;
   if (pre) {
-    if (p.logits_dtype == DG_BF16)
-      selfcond_pmat_kernel<DG_BF16><<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
-    else
-      selfcond_pmat_kernel<DG_F32><<<(unsigned)rows, 256, 0, s>>>(a, reinterpret_cast<uint4 *>(ws), plan.p_ld);
+    uint4 *pw = reinterpret_cast<uint4 *>(ws);
+    if (p.logits_dtype == DG_BF16) {
+      if (cap) selfcond_pmat_kernel<DG_BF16, true><<<(unsigned)rows, 256, 0, s>>>(a, pw, plan.p_ld);
+      else selfcond_pmat_kernel<DG_BF16, false><<<(unsigned)rows, 256, 0, s>>>(a, pw, plan.p_ld);
+    } else {
+      if (cap) selfcond_pmat_kernel<DG_F32, true><<<(unsigned)rows, 256, 0, s>>>(a, pw, plan.p_ld);
+      else selfcond_pmat_kernel<DG_F32, false><<<(unsigned)rows, 256, 0, s>>>(a, pw, plan.p_ld);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

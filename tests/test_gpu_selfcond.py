@@ -1,7 +1,10 @@
 """GPU parity of dg_selfcond_embed (the tcgen05 p.E contraction) against the
 fp64 oracle: ragged M / N / K tiles, split-K and single-pass plans, both
-logit dtypes, fp32 and bf16 outputs, padded E rows, rows that do not feed the
-next step, and the one-hot case that must return embedding rows exactly."""
+logit dtypes, fp32 and bf16 outputs, padded E rows, the three ways the A
+operand arrives (bf16 logits by TMA with the rebuild in the GEMM, p
+materialised first for fp32 logits and strides off 16 bytes, and producer
+loads for bf16 rows on a base off a 16-byte boundary), rows that do not feed
+the next step, and the one-hot case that must return embedding rows exactly."""
 
 import numpy as np
 import pytest
@@ -98,3 +101,30 @@ def test_rows_that_do_not_feed_are_zero():
     assert torch.count_nonzero(out[0]).item() > 0
     snap = st.snapshot()
     assert snap["sc_valid"].tolist() == [1, 0, 0, 0]
+
+
+@pytest.mark.parametrize("split", [False, True], ids=["one-pass", "split-K"])
+def test_selfcond_bf16_rows_off_a_16_byte_boundary(split):
+    # a 16-byte-multiple stride on a base address 2 bytes past a 16-byte
+    # boundary: the one input the GEMM's producers still load themselves
+    # (fp32 logits and strides off 16 bytes materialise p first)
+    B, C = 2, 128
+    V, d, ld = (20000, 256, 20008) if split else (1000, 64, 1008)
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, logits_ld=ld, seed=21,
+                  entropy_budget=50.0, conf_threshold=-1.0, stable_k=3, step_cap=1000)
+    temps = [0.75, 1.2]
+    st = make_state(p, [dg.DG_PHASE_DENOISE] * B, temperatures=temps)
+    src = syn.boosted_logits(B * C, V, seed=5, dtype=torch.bfloat16, device="cuda", ld=ld).reshape(-1)
+    flat = torch.empty(src.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    logits = flat[1:1 + src.numel()]
+    logits.copy_(src)
+    assert logits.data_ptr() % 16 == 2
+    E = syn.embedding(V, d, seed=7, device="cuda")
+    out = _run(p, st, logits, E)
+    assert int(st.device_status.item()) == 0
+    got = out.cpu().numpy()
+    Eh = E.float().cpu().numpy().astype(np.float64)
+    zh = src.view(B, C, ld)[:, :, :V].float().cpu().numpy()
+    for r in range(B):
+        ref = oracle_selfcond_rows(zh[r], float(np.float32(temps[r])), Eh)
+        selfcond_check(got[r * C:(r + 1) * C], ref)

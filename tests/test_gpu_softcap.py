@@ -3,7 +3,7 @@ on the self-conditioning feed ("The Annotated DiffusionGemma", "Logit
 Softcapping" and the model's forward pass) against the fp64 oracle: the
 sampler step on bf16 and fp32 logits, aligned and unaligned rows, a mild and a
 hard cap; infinite logits (capped to +-c) and NaN rows; the self-conditioning
-feed through the TMA, producer-load, split-K and single-pass plans; and the
+feed through the TMA, materialised-p, split-K and single-pass plans; and the
 scale alone, which must be an exact fp32 product."""
 
 import numpy as np
