@@ -40,7 +40,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t denoise_ws_bytes(const dg_params *p) {
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
-  const VocabChunking vc = vocab_chunking(n_pos, p->vocab);
+  const VocabChunking vc = vocab_chunking(n_pos, p->vocab, vocab_per_group(*p));
   return round_up((size_t)n_pos * (size_t)vc.n_chunks * sizeof(Partial), 256);
 }
 
@@ -193,7 +193,7 @@ int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st, 
   if (dv != DG_OK) return dv;
   cudaGetLastError();
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
-  const VocabChunking vc = vocab_chunking(n_pos, p->vocab);
+  const VocabChunking vc = vocab_chunking(n_pos, p->vocab, vocab_per_group(*p));
   Partial *part = reinterpret_cast<Partial *>(ws);
   if (launch_vocab_pass(*p, logits, *st, part, vc.chunk, vc.n_chunks, stream) != cudaSuccess)
     return DG_ERR_CUDA;

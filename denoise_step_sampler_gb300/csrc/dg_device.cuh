@@ -154,7 +154,8 @@ struct VocabChunking {
   int32_t chunk;     // elements per chunk (a multiple of 1024)
   int32_t n_chunks;  // chunks per position
 };
-__host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V) {
+__host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V,
+                                                        bool per_group) {
   // Few, long chunks: each warp's start (stream keys, the warm start of the
   // Gumbel screen, the first rounds' exact evaluations) is amortised over its
   // chunk, and a count that divides 8 keeps the eight warps of a CTA on whole
@@ -162,9 +163,13 @@ __host__ __device__ inline VocabChunking vocab_chunking(int64_t n_pos, int32_t V
   // follow timings of the pass on a GB300 at V = 262,144 for 256 to 32,768
   // positions (2, 4, 8 and 16 chunks tried at each): 8 chunks for up to 1,216
   // positions, 4 up to 9,728, 2 beyond; never below 2048 logits per chunk.
+  // Rows that take the per-group path (fp32 logits, bf16 rows whose stride
+  // is not a multiple of 16 bytes) load each group with plain loads; at few
+  // positions they are latency-bound, and 16 requested chunks (13 at
+  // V = 50,257) beat 8 by 13 % at 256 positions.
   int64_t nc = 2;
   if (n_pos <= 9728) nc = 4;
-  if (n_pos <= 1216) nc = 8;
+  if (n_pos <= 1216) nc = per_group ? 16 : 8;
   while (nc > 1 && ((int64_t)V + nc - 1) / nc < 2048) nc >>= 1;
   // chunks start on multiples of 1024 indices, so that every vocabulary
   // segment of the segmented Gumbel-max rule (32 indices inside one

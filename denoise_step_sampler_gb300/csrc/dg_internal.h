@@ -54,6 +54,12 @@ struct SelfcondPlan {
 // selfcond_materialises) the plan also holds the materialised p.
 SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, int64_t l2_bytes,
                            bool materialise);
+// Whether the vocabulary pass reads its rows group by group with plain loads
+// (fp32 logits, or bf16 rows whose stride is not a multiple of 16 bytes)
+// rather than through its load ring; the chunk count depends on it.
+inline bool vocab_per_group(const dg_params &p) {
+  return p.logits_dtype != DG_BF16 || (p.logits_ld * 2) % 16 != 0;
+}
 // Whether the self-conditioning call materialises p before the GEMM: a
 // softcapped feed, or logits the GEMM cannot copy by TMA (fp32, or bf16 rows
 // whose stride is not a multiple of 16 bytes).

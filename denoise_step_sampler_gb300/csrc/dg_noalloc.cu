@@ -95,7 +95,7 @@ extern "C" int dg_denoise_step_noalloc(const dg_params *p, const void *logits, c
   const int rc = dg::denoise_args_ok(p, logits, st);
   if (rc != DG_OK) return rc;
   const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
-  const dg::VocabChunking vc = dg::vocab_chunking(n_pos, p->vocab);
+  const dg::VocabChunking vc = dg::vocab_chunking(n_pos, p->vocab, dg::vocab_per_group(*p));
   if (n_pos * (int64_t)vc.n_chunks > (int64_t)kScratchRecords) return DG_ERR_SCRATCH_LIMIT;
   const int dv = dg::device_ok();
   if (dv != DG_OK) return dv;
