@@ -174,12 +174,6 @@ __device__ __forceinline__ void seg_add(Lane &L, int32_t k, float mass, const Ke
 // r+2 are in flight, without holding registers.
 constexpr int kStages = 3;
 constexpr int kRingBytes = kWarps * kStages * 128 * 16;  // 48 KB per CTA
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   (uint32_t)__cvta_generic_to_shared(dst)),
-               "l"(src)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async16s(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
