@@ -128,3 +128,30 @@ def test_selfcond_bf16_rows_off_a_16_byte_boundary(split):
     for r in range(B):
         ref = oracle_selfcond_rows(zh[r], float(np.float32(temps[r])), Eh)
         selfcond_check(got[r * C:(r + 1) * C], ref)
+
+
+@pytest.mark.parametrize("V,d", [(500, 32), (60000, 256)], ids=["one-pass", "split-K"])
+def test_fp32_rows_that_do_not_feed_are_zero_whatever_the_workspace_holds(V, d):
+    # fp32 logits take the materialised-p route, which never writes the p of
+    # rows that do not feed; the workspace is filled with NaN bytes first
+    B, C = 4, 64
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_F32, seed=4,
+                  entropy_budget=50.0, conf_threshold=-1.0, stable_k=1, step_cap=2)
+    st = make_state(p, [dg.DG_PHASE_DENOISE, dg.DG_PHASE_PREFILL, dg.DG_PHASE_IDLE,
+                        dg.DG_PHASE_DENOISE], temperatures=[0.9, 1, 1, 1])
+    st.step[3] = 1  # reaches the cap: converges, does not feed
+    logits = syn.boosted_logits(B * C, V, seed=1, dtype=torch.float32, device="cuda").reshape(-1)
+    E = syn.embedding(V, d, seed=6, device="cuda")
+    ws = torch.full((max(16, dg.dg_workspace_bytes(p, d)),), 0xFF, dtype=torch.uint8, device="cuda")
+    dg.dg_denoise_step(p, logits, st, ws)
+    ws.fill_(0xFF)
+    out = torch.full((B * C, d), float("nan"), dtype=torch.float32, device="cuda")
+    dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+    torch.cuda.synchronize()
+    assert int(st.device_status.item()) == 0
+    assert st.snapshot()["sc_valid"].tolist() == [1, 0, 0, 0]
+    got = out.view(B, C, d)
+    assert torch.count_nonzero(got[1:]).item() == 0
+    zh = logits.view(B, C, V)[0].cpu().numpy().astype(np.float64)
+    ref = oracle_selfcond_rows(zh, float(np.float32(0.9)), E.float().cpu().numpy().astype(np.float64))
+    selfcond_check(got[0].cpu().numpy(), ref)
