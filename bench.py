@@ -442,13 +442,13 @@ def _selfcond_launches(p, d):
     reduction when the library splits the vocabulary (its fp32 partial sums,
     [splits][rows][d], are the workspace beyond the sampler's and beyond a
     materialised p); and the kernel that materialises p (bf16 rows of V
-    rounded up to 8, 256-byte aligned) for a softcapped feed or for logits the
+    rounded up to 8, 256-byte aligned) for a softcapped feed, for logits the
     GEMM cannot copy by TMA (fp32, or bf16 rows whose stride is not a multiple
-    of 16 bytes)."""
+    of 16 bytes), and from 1,024 positions on."""
     import denoise_step_sampler_gb300 as dg
     rows = p.batch * p.canvas_len
     ld = p.logits_ld or p.vocab
-    if p.softcap > 0 or p.logits_dtype != dg.DG_BF16 or (ld * 2) % 16:
+    if p.softcap > 0 or p.logits_dtype != dg.DG_BF16 or (ld * 2) % 16 or rows >= 1024:
         p_bytes = (rows * ((p.vocab + 7) // 8 * 8) * 2 + 255) // 256 * 256
         return 2 + (1 if dg.dg_workspace_bytes(p, d) > p_bytes else 0)
     return 2 if dg.dg_workspace_bytes(p, d) > dg.dg_workspace_bytes(p, 0) else 1

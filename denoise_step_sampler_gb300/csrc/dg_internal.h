@@ -61,10 +61,16 @@ inline bool vocab_per_group(const dg_params &p) {
   return p.logits_dtype != DG_BF16 || (p.logits_ld * 2) % 16 != 0;
 }
 // Whether the self-conditioning call materialises p before the GEMM: a
-// softcapped feed, or logits the GEMM cannot copy by TMA (fp32, or bf16 rows
-// whose stride is not a multiple of 16 bytes).
+// softcapped feed, logits the GEMM cannot copy by TMA (fp32, or bf16 rows
+// whose stride is not a multiple of 16 bytes), or 1,024 positions (four row
+// tiles) and more.  At V = 262,144, d = 2,816 the pass that writes p plus the
+// GEMM on it (no rebuild in its producers) took 2 % (4 canvases) to 8 %
+// (64 canvases) less than the rebuilding GEMM alone, and 4 % less at 128;
+// at 1 and 2 canvases, where the GEMM waits on the E reads, it took 4-9 %
+// more.
 inline bool selfcond_materialises(const dg_params &p) {
-  return p.softcap > 0.f || p.logits_dtype != DG_BF16 || (p.logits_ld * 2) % 16 != 0;
+  return p.softcap > 0.f || p.logits_dtype != DG_BF16 || (p.logits_ld * 2) % 16 != 0 ||
+         (int64_t)p.batch * p.canvas_len >= 1024;
 }
 
 // SMs of the current device (cached per device); 152, the GB300's count, when

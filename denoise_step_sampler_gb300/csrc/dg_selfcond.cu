@@ -742,9 +742,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // so that the GEMM's tiles need no rebuild.  Used where the rebuild would be
 // slow: softcapped feeds (rebuilt in the GEMM, every column tile, 11 at
 // d = 2,816, would cap each logit again, three transcendental operations per
-// element each time), and logits the GEMM cannot copy by TMA (fp32, or bf16
-// rows whose stride is not a multiple of 16 bytes), which its producers would
-// otherwise load one stage ahead with plain loads.  One CTA per row; each
+// element each time), logits the GEMM cannot copy by TMA (fp32, or bf16 rows
+// whose stride is not a multiple of 16 bytes), which its producers would
+// otherwise load one stage ahead with plain loads, and batches of four row
+// tiles and more, where the rebuild's shared-memory traffic costs the GEMM
+// more than this pass costs.  One CTA per row; each
 // thread keeps four 16-byte loads in flight.  Rows that do not feed are not
 // written: the GEMM's epilogue writes zeros for them whatever their A rows
 // hold (row q of the product depends on row q of p alone).

@@ -171,9 +171,10 @@ typedef struct {
  * split's slice of E fits in L2); query it with the device current that the
  * calls will run on.  With d > 0 it
  * includes the feed's materialised probabilities, B*C rows of V rounded up to
- * 8 bf16 (about B*C*V*2 bytes: 1.07 GB for 8 x 256 positions at V = 262,144),
- * when p->softcap > 0 or when the logits are fp32 or bf16 rows whose stride
- * (logits_ld * 2 bytes) is not a multiple of 16. */
+ * 8 bf16 (about B*C*V*2 bytes: 1.07 GB for 8 x 256 positions at V = 262,144,
+ * 17.2 GB for 128 x 256), when B*C >= 1024, when p->softcap > 0, or when the
+ * logits are fp32 or bf16 rows whose stride (logits_ld * 2 bytes) is not a
+ * multiple of 16. */
 size_t dg_workspace_bytes(const dg_params *p, int32_t d);
 
 /* Stand-alone canvas initialisation (the prefill case) of the rows r with
@@ -214,11 +215,11 @@ int dg_denoise_step(const dg_params *p, const void *logits, const dg_state *st,
  * `d`: 16 <= d, d % 16 == 0.  `out`: device [B*C][d] of out_dtype (DG_F32 or
  * DG_BF16).  `ws`: at least dg_workspace_bytes(p, d) bytes.  Products run on
  * the tensor cores in bf16 with fp32 accumulation.  One to three kernel
- * launches: for a softcapped feed, fp32 logits, or bf16 rows whose stride is
- * not a multiple of 16 bytes, a first kernel writes the probabilities to `ws`
- * once and the GEMM reads them from there (otherwise the GEMM rebuilds them
- * from the logits tile by tile); the GEMM; a split-K reduction when the
- * vocabulary is split. */
+ * launches: from 1,024 positions on, for a softcapped feed, for fp32 logits,
+ * or for bf16 rows whose stride is not a multiple of 16 bytes, a first kernel
+ * writes the probabilities to `ws` once and the GEMM reads them from there
+ * (otherwise the GEMM rebuilds them from the logits tile by tile); the GEMM;
+ * a split-K reduction when the vocabulary is split. */
 int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st,
                       const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                       void *ws, size_t ws_bytes, cudaStream_t stream);

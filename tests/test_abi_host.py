@@ -145,18 +145,24 @@ def test_anneal_arguments_are_rejected_on_host(L):
 
 
 def test_workspace_follows_the_split_plan(L):
-    # the self-conditioning workspace is [splits][B*C][d] fp32 partial sums
-    # (plus the materialised p of a softcapped feed); on a 152-SM part with
+    # the self-conditioning workspace is the materialised p (bf16 rows of V
+    # rounded up to 8, from 1,024 positions on, and for softcapped feeds)
+    # followed by [splits][B*C][d] fp32 partial sums; on a 152-SM part with
     # 129 MiB of L2 (the values used when no device can be queried):
     #  - 8 and 64 canvases take the split count that fills the SMs in whole
     #    waves (5 and 3);
     #  - 128 canvases (more than 64 row tiles of 256) split further, until one
     #    split's slice of E fits in L2: 11 splits (10 would leave 148 MB)
     V, d = 262144, 2816
+    p_bytes = lambda B: (B * 256 * V * 2 + 255) // 256 * 256
     for B, splits in ((8, 5), (64, 3), (128, 11)):
         p = dg.Params(batch=B, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16)
-        assert dg.dg_workspace_bytes(p, d) == splits * B * 256 * d * 4, B
+        assert dg.dg_workspace_bytes(p, d) == p_bytes(B) + splits * B * 256 * d * 4, B
     assert V * d * 2 // 10 > 135528448 >= V * d * 2 // 11
-    capped = dg.Params(batch=8, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16, softcap=30.0)
-    p_bytes = (8 * 256 * V * 2 + 255) // 256 * 256
-    assert dg.dg_workspace_bytes(capped, d) == p_bytes + 5 * 8 * 256 * d * 4
+    # two canvases rebuild p inside the GEMM: partial sums only, 48 splits
+    # (22 tiles x 48 = 1,056 CTAs, 99 % of 7 waves)
+    two = dg.Params(batch=2, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16)
+    ws2 = dg.dg_workspace_bytes(two, d)
+    assert ws2 == 48 * 2 * 256 * d * 4
+    capped = dg.Params(batch=2, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16, softcap=30.0)
+    assert dg.dg_workspace_bytes(capped, d) == p_bytes(2) + ws2
