@@ -277,13 +277,19 @@ def run_ours(args, rank, world, dev):
     st.phase.fill_(dg.DG_PHASE_DENOISE)
     st.temperature.fill_(T)
     st.request_id.copy_(torch.tensor(shard_request_ids(B, rank), device=dev))
-    ws = torch.empty(max(16, dg.dg_workspace_bytes(p, d)), dtype=torch.uint8, device=dev)
+    fused = not args.two_calls
+    ws_n = dg.dg_workspace_bytes_feed(p, d) if fused else dg.dg_workspace_bytes(p, d)
+    ws = torch.empty(max(16, ws_n), dtype=torch.uint8, device=dev)
     out = torch.empty((B * C, d), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(lg):
-        dg.dg_denoise_step(p, lg, st, ws)
-        dg.dg_selfcond_embed(p, lg, st, E, out, ws)
+        # one pass of the whole path: the fused call, or the two calls in turn
+        if fused:
+            dg.dg_denoise_step_feed(p, lg, st, E, out, ws)
+        else:
+            dg.dg_denoise_step(p, lg, st, ws)
+            dg.dg_selfcond_embed(p, lg, st, E, out, ws)
 
     for _ in range(args.warmup):
         step(logits)
@@ -307,16 +313,26 @@ def run_ours(args, rank, world, dev):
         if flush is not None:
             flush.fill_(k & 0xFF)
         ev[k][0].record(stream)
-        dg.dg_denoise_step(p, logits, st, ws)
-        ev[k][1].record(stream)
-        dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+        step(logits)
         ev[k][2].record(stream)
+    # The per-call times behind the two rooflines: the same workload through
+    # the two calls (dg_denoise_step, then dg_selfcond_embed), timed in turn
+    # right after the steps (the fused call cannot be split by events).
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for k in range(K):
+        if flush is not None:
+            flush.fill_(k & 0xFF)
+        ev2[k][0].record(stream)
+        dg.dg_denoise_step(p, logits, st, ws)
+        ev2[k][1].record(stream)
+        dg.dg_selfcond_embed(p, logits, st, E, out, ws)
+        ev2[k][2].record(stream)
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     step_ms = [e[0].elapsed_time(e[2]) for e in ev]
     ms = sum(step_ms)
-    ms_sampler = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    ms_sc = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    ms_sampler = sum(e[0].elapsed_time(e[1]) for e in ev2) / K
+    ms_sc = sum(e[1].elapsed_time(e[2]) for e in ev2) / K
     status = int(st.device_status.item())
 
     ms_e2e, Ke = float('nan'), 0
@@ -384,7 +400,7 @@ def run_ours(args, rank, world, dev):
     sc_tflops = flops / (ms_sc / 1e3) / 1e12
     logit_bytes = n_pos * V * esz
     sampler_gbs = logit_bytes / (ms_sampler / 1e3) / 1e9
-    launches_per_step = 2 + _selfcond_launches(p, d)
+    launches_per_step = (3 + _feed_launches(p, d)) if fused else (2 + _selfcond_launches(p, d))
     line = {
         "metric": METRIC, "value": value, "unit": "positions/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms / K,
@@ -402,8 +418,12 @@ def run_ours(args, rank, world, dev):
                    "parallelism": f"replicas x{world} (independent requests per GPU)",
                    "accept_rule": args.accept_rule, "stop_rule": args.stop_rule,
                    "softcap": args.softcap, "embed_scale": args.embed_scale,
-                   "sample_rule": args.sample_rule},
-        "roofline": {"bound": "tensor", "kernel": "dg_selfcond_embed (tcgen05 GEMM + split-K reduce)",
+                   "sample_rule": args.sample_rule,
+                   "step_call": "dg_denoise_step_feed" if fused else
+                                "dg_denoise_step + dg_selfcond_embed"},
+        "roofline": {"bound": "tensor",
+                     "kernel": "dg_selfcond_embed (p materialisation or rebuild, tcgen05 GEMM, split-K "
+                               "reduce), timed on the two-call path over the same workload",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16, "frac_of_burst": sc_tflops / bf16_burst,
                      "traffic": None if args.batch else traffic_for("dg_selfcond_embed", args.workload),
@@ -411,7 +431,9 @@ def run_ours(args, rank, world, dev):
                          src, "sustained" if long_region else "burst", ms / 1e3),
                      "flops_per_launch": flops,
                      "ms_per_launch": ms_sc},
-        "roofline_sampler": {"bound": "hbm", "kernel": "dg_denoise_step (vocab pass + canvas step)",
+        "roofline_sampler": {"bound": "hbm",
+                             "kernel": "dg_denoise_step (vocab pass + canvas step), timed on the "
+                                       "two-call path over the same workload",
                              "achieved": sampler_gbs, "peak": hbm, "unit": "GB/s",
                              "frac": sampler_gbs / hbm,
                              "traffic": None if args.batch else traffic_for("dg_denoise_step", args.workload),
@@ -422,7 +444,7 @@ def run_ours(args, rank, world, dev):
                 "h2d_bytes_per_step": logit_bytes,
                 "d2h_bytes_per_step": int(out.numel() * 4 + st.canvas.numel() * 4),
                 "steps": Ke},
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * K + (2 + _selfcond_launches(p, d)) * K,
         "device_status": status,
     }
     if not args.no_cpu_baseline:
@@ -452,6 +474,25 @@ def _selfcond_launches(p, d):
         p_bytes = (rows * ((p.vocab + 7) // 8 * 8) * 2 + 255) // 256 * 256
         return 2 + (1 if dg.dg_workspace_bytes(p, d) > p_bytes else 0)
     return 2 if dg.dg_workspace_bytes(p, d) > dg.dg_workspace_bytes(p, 0) else 1
+
+
+def _feed_launches(p, d):
+    """Kernel launches of one dg_denoise_step_feed call besides the vocabulary
+    pass, the canvas step and the GEMM: the materialisation pass (it completes
+    the rows the vocabulary pass could not write and returns at once for the
+    others) and the split-K reduction when the vocabulary is split (the same
+    split plan as the two calls).  Inputs the fusion does not take run the two
+    calls."""
+    import denoise_step_sampler_gb300 as dg
+    ld = p.logits_ld or p.vocab
+    rows = p.batch * p.canvas_len
+    unaligned = (ld * 2) % 16 != 0
+    if p.logits_dtype != dg.DG_BF16 or p.softcap > 0 or unaligned or \
+            p.sample_rule != dg.DG_SAMPLE_SEGMENTED:
+        return _selfcond_launches(p, d) - 1
+    two_call_materialises = rows >= 1024
+    has_reduce = _selfcond_launches(p, d) - 1 - (1 if two_call_materialises else 0)
+    return 1 + has_reduce
 
 
 def run_graph_loop(args, dev):
@@ -703,6 +744,9 @@ def main():
     ap.add_argument("--mode", default="step", choices=["step", "graph-loop", "mixed-loop"],
                     help="step: the throughput line (default); graph-loop: one-canvas loop "
                          "latency; mixed-loop: the 32-request mixed-phase loop")
+    ap.add_argument("--two-calls", action="store_true",
+                    help="time dg_denoise_step + dg_selfcond_embed as the step instead of the "
+                         "fused dg_denoise_step_feed")
     ap.add_argument("--softcap", type=float, default=0.0,
                     help="logit softcap c (c tanh(z / c) before the pass); 0 = off")
     ap.add_argument("--embed-scale", type=float, default=0.0,

@@ -22,6 +22,7 @@ __all__ = [
     "DG_DEV_BAD_TOKEN", "DG_DEV_WAIT_TIMEOUT", "DG_DEV_BAD_PHASE",
     "Params", "State", "DgError", "lib", "library_path",
     "dg_workspace_bytes", "dg_init_canvas", "dg_denoise_step", "dg_selfcond_embed",
+    "dg_denoise_step_feed", "dg_workspace_bytes_feed",
     "dg_commit", "dg_status_string", "dg_debug_wait_record", "dg_denoise_step_noalloc",
     "DG_ERR_SCRATCH_LIMIT", "load",
 ]
@@ -91,6 +92,9 @@ def load(path: str) -> ctypes.CDLL:
     L.dg_denoise_step.restype = ctypes.c_int
     L.dg_selfcond_embed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
     L.dg_selfcond_embed.restype = ctypes.c_int
+    L.dg_workspace_bytes_feed.argtypes, L.dg_workspace_bytes_feed.restype = [P, i32], sz
+    L.dg_denoise_step_feed.argtypes = [P, vp, S, vp, i32, i64, vp, i32, vp, sz, vp]
+    L.dg_denoise_step_feed.restype = ctypes.c_int
     L.dg_status_string.argtypes, L.dg_status_string.restype = [ctypes.c_int], ctypes.c_char_p
     L.dg_denoise_step_noalloc.argtypes = [P, vp, S, vp]
     L.dg_denoise_step_noalloc.restype = ctypes.c_int
@@ -315,3 +319,28 @@ def dg_selfcond_embed(params: Params, logits: torch.Tensor, state: State, E: tor
     _check(lib().dg_selfcond_embed(ctypes.byref(params.c()), _ptr(logits), ctypes.byref(state.c()),
                                    _ptr(E), int(d), int(E.stride(0)), _ptr(out), odt, ws_ptr, ws_n,
                                    _stream_ptr(stream)), "dg_selfcond_embed")
+
+
+def dg_workspace_bytes_feed(params: Params, d: int) -> int:
+    return int(lib().dg_workspace_bytes_feed(ctypes.byref(params.c()), int(d)))
+
+
+def dg_denoise_step_feed(params: Params, logits: torch.Tensor, state: State, E: torch.Tensor,
+                         out: torch.Tensor, workspace: torch.Tensor, stream=None):
+    _logits_ok(params, logits)
+    if E.dtype != torch.bfloat16 or E.dim() != 2 or E.stride(1) != 1 or E.shape[0] != params.vocab:
+        raise ValueError("E: want bf16 [V, d] with unit column stride")
+    d = E.shape[1]
+    if out.dtype == torch.float32:
+        odt = DG_F32
+    elif out.dtype == torch.bfloat16:
+        odt = DG_BF16
+    else:
+        raise ValueError("out: want float32 or bfloat16")
+    if out.numel() != params.batch * params.canvas_len * d or not out.is_contiguous():
+        raise ValueError("out: want contiguous [batch * canvas_len, d]")
+    ws_n = workspace.numel() * workspace.element_size()
+    _check(lib().dg_denoise_step_feed(ctypes.byref(params.c()), _ptr(logits),
+                                      ctypes.byref(state.c()), _ptr(E), int(d), int(E.stride(0)),
+                                      _ptr(out), odt, _ptr(workspace), ws_n, _stream_ptr(stream)),
+           "dg_denoise_step_feed")

@@ -226,6 +226,77 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
   return DG_OK;
 }
 
+namespace {
+// The fused step writes the feed's operand from the vocabulary pass for bf16
+// rows on 16-byte boundaries under the segmented rule without a softcap;
+// other inputs run the two calls in turn.
+bool feed_fusable(const dg_params &p, const void *logits) {
+  return p.logits_dtype == DG_BF16 && !(p.softcap > 0.f) &&
+         p.sample_rule == DG_SAMPLE_SEGMENTED && (p.logits_ld * 2) % 16 == 0 &&
+         aligned(logits, 16);
+}
+// Workspace of the fused step: [vocabulary-pass records][per-position R]
+// [the operand rows (the self-cond plan's p) | split-K partial sums].
+struct FeedLayout {
+  size_t off_R, off_sc, total;
+  SelfcondPlan plan;
+};
+FeedLayout feed_layout(const dg_params &p, int32_t d) {
+  FeedLayout f;
+  const int64_t rows = (int64_t)p.batch * p.canvas_len;
+  f.off_R = denoise_ws_bytes(&p);
+  f.off_sc = round_up(f.off_R + (size_t)rows * sizeof(float), 256);
+  f.plan = selfcond_plan(rows, p.vocab, d, device_sm_count(), device_l2_bytes(), true);
+  f.total = f.off_sc + f.plan.ws_bytes;
+  return f;
+}
+}  // namespace
+
+size_t dg_workspace_bytes_feed(const dg_params *p, int32_t d) {
+  if (!params_ok(p) || d < 16 || d % 16 != 0) return 0;
+  const size_t fused = feed_layout(*p, d).total;
+  const size_t apart = dg_workspace_bytes(p, d);
+  return fused > apart ? fused : apart;
+}
+
+int dg_denoise_step_feed(const dg_params *p, const void *logits, const dg_state *st,
+                         const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
+                         void *ws, size_t ws_bytes, cudaStream_t stream) {
+  const int rc = denoise_args_ok(p, logits, st);
+  if (rc != DG_OK) return rc;
+  if (!E || !out || d < 16 || d % 16 != 0 || ld_E < d || (ld_E * 2) % 16 != 0)
+    return DG_ERR_INVALID_ARG;
+  if (out_dtype != DG_F32 && out_dtype != DG_BF16) return DG_ERR_INVALID_ARG;
+  if (!aligned(E, 16) || !aligned(out, 16)) return DG_ERR_INVALID_ARG;
+  if (!st->sc_valid || !st->m || !st->s) return DG_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < dg_workspace_bytes_feed(p, d) || !aligned(ws, 16)) return DG_ERR_WORKSPACE;
+  const int dv = device_ok();
+  if (dv != DG_OK) return dv;
+  if (!feed_fusable(*p, logits)) {
+    const int r1 = dg_denoise_step(p, logits, st, ws, ws_bytes, stream);
+    if (r1 != DG_OK) return r1;
+    return dg_selfcond_embed(p, logits, st, E, d, ld_E, out, out_dtype, ws, ws_bytes, stream);
+  }
+  cudaGetLastError();
+  const FeedLayout f = feed_layout(*p, d);
+  char *w = reinterpret_cast<char *>(ws);
+  Partial *part = reinterpret_cast<Partial *>(w);
+  float *feed_R = reinterpret_cast<float *>(w + f.off_R);
+  void *ws_sc = w + f.off_sc;
+  const int64_t n_pos = (int64_t)p->batch * p->canvas_len;
+  const VocabChunking vc = vocab_chunking(n_pos, p->vocab, false);
+  if (launch_vocab_pass_feed(*p, logits, *st, part, vc.chunk, vc.n_chunks,
+                             reinterpret_cast<uint4 *>(ws_sc), f.plan.p_ld / 8,
+                             stream) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (launch_canvas_step(*p, *st, part, vc.n_chunks, 0, nullptr, stream, feed_R) != cudaSuccess)
+    return DG_ERR_CUDA;
+  if (launch_selfcond(*p, logits, *st, E, d, ld_E, out, out_dtype, ws_sc, f.plan, stream,
+                      feed_R) != cudaSuccess)
+    return DG_ERR_CUDA;
+  return DG_OK;
+}
+
 int dg_debug_wait_record(uint32_t out[4]) {
   if (!out) return DG_ERR_INVALID_ARG;
   if (dg_selfcond_wait_record(out) != cudaSuccess) return DG_ERR_CUDA;

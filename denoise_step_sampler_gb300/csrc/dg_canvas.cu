@@ -46,6 +46,7 @@ struct CanvasArgs {
   int32_t merge_threads;  // threads per position in the chunk merge (1, 2 or 4)
   int mode;
   const uint8_t *row_mask;
+  float *feed_R;  // fused step: per position, the operand's reference R, or NaN (fall back)
 };
 
 __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
@@ -127,11 +128,15 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
     uint32_t fl = 0;
     float zmax = -INFINITY, b2 = -INFINITY, S = 0.f, Tt = 0.f;
     int32_t pam = -1, pcand = -1;
+    int feed_all = 1;           // every chunk wrote its operand columns
+    float feed_R = -INFINITY;   // their common reference
     if (i < C) {
       const Partial *P = a.part + (size_t)(base + i) * a.n_chunks;
       for (int ch = sub; ch < a.n_chunks; ch += mt) {
         const Partial q = P[ch];
         fl |= q.flags;
+        if ((q.flags & kPartFeed) == 0) feed_all = 0;
+        feed_R = fmaxf(feed_R, __uint_as_float(q.pad));
         if (q.zmax > zmax || (q.zmax == zmax && q.am >= 0 && (pam < 0 || q.am < pam))) {
           if (q.zmax > zmax && S > 0.f) {  // the running maximum grows
             const float d = ceilf(zmax * c) - ceilf(q.zmax * c);
@@ -162,6 +167,8 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       const float ob = __shfl_xor_sync(0xFFFFFFFFu, b2, off);
       const int32_t oc = __shfl_xor_sync(0xFFFFFFFFu, pcand, off);
       fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, off);
+      feed_all &= __shfl_xor_sync(0xFFFFFFFFu, feed_all, off);
+      feed_R = fmaxf(feed_R, __shfl_xor_sync(0xFFFFFFFFu, feed_R, off));
       const float nz = fmaxf(zmax, oz);
       if (nz != -INFINITY) {
         float ns = 0.f, nt2 = 0.f;
@@ -210,6 +217,12 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
       st.entropy[base + i] = Hf;
       st.argmax[base + i] = ok ? pam : 0;
       st.cand[base + i] = ok ? pcand : 0;
+      if (a.feed_R) {
+        // the operand 2^(z c - R) holds this position's distribution when its
+        // maximum term lies within 2^+-kFeedSpan
+        const bool fok = ok && feed_all && fabsf(zmax * c - feed_R) <= kFeedSpan;
+        a.feed_R[base + i] = fok ? feed_R : NAN;
+      }
     }
   }
   __syncthreads();
@@ -326,7 +339,7 @@ __global__ void __launch_bounds__(kMaxC) canvas_step_kernel(CanvasArgs a) {
 
 cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Partial *part,
                                int32_t n_chunks, int mode, const uint8_t *row_mask,
-                               cudaStream_t s) {
+                               cudaStream_t s, float *feed_R) {
   int threads = 32;
   while (threads < p.canvas_len) threads <<= 1;
   // spread the chunk merge over up to 4 threads per position when there are
@@ -353,6 +366,7 @@ cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Par
   a.merge_threads = mt;
   a.mode = mode;
   a.row_mask = row_mask;
+  a.feed_R = feed_R;
   canvas_step_kernel<<<p.batch, threads, 0, s>>>(a);
   return cudaGetLastError();
 }

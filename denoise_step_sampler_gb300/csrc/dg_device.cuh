@@ -146,7 +146,17 @@ struct alignas(16) Partial {
   uint32_t flags;
   uint32_t pad;
 };
-enum : uint32_t { kPartNaN = 1u, kPartPInf = 2u, kPartBadT = 4u };
+enum : uint32_t { kPartNaN = 1u, kPartPInf = 2u, kPartBadT = 4u, kPartFeed = 8u };
+// The fused step (dg_denoise_step_feed): the vocabulary pass writes the
+// feed's operand 2^(z c - R) as bf16 while it streams the logits, with R the
+// whole number ceil(m' log2 e) + kFeedMargin from the position's previous
+// maximum m' (dg_state.m before this step); a chunk that wrote all of its
+// columns sets kPartFeed and leaves R in its record's pad word.  A position
+// keeps that operand when its new maximum satisfies |zmax c - R| <= kFeedSpan:
+// the largest term is then within 2^+-96 (bf16 spans 2^-133 .. 2^127), and no
+// term that matters underflows.
+constexpr float kFeedMargin = 32.f;
+constexpr float kFeedSpan = 96.f;
 
 // Chunking of the vocabulary for the vocabulary pass: a pure function of the
 // sizes, shared by the workspace query and the launch.

@@ -33,9 +33,17 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
 
 // K2: per-canvas merge + acceptance + re-noise + convergence + phase machine.
 // mode 0: every row by its phase; 1: init rows in row_mask; 2: commit rows in row_mask.
+// The fused step's vocabulary pass: as launch_vocab_pass (bf16 rows on
+// 16-byte boundaries, segmented rule, no softcap) and it also writes the
+// feed's operand, rows of feed_ld8 16-byte words at feed_p.
+cudaError_t launch_vocab_pass_feed(const dg_params &p, const void *logits, const dg_state &st,
+                                   Partial *part, int32_t chunk, int32_t n_chunks,
+                                   uint4 *feed_p, int64_t feed_ld8, cudaStream_t s);
+// feed_R (fused step only, else null): per position, the reference R of the
+// operand the vocabulary pass wrote, or NaN where the position must fall back.
 cudaError_t launch_canvas_step(const dg_params &p, const dg_state &st, const Partial *part,
                                int32_t n_chunks, int mode, const uint8_t *row_mask,
-                               cudaStream_t s);
+                               cudaStream_t s, float *feed_R = nullptr);
 
 // K4: self-conditioning GEMM (tcgen05 / TMEM).
 struct SelfcondPlan {
@@ -80,9 +88,13 @@ int32_t device_sm_count();
 // device can be queried.
 constexpr int64_t kGB300L2Bytes = 135528448;
 int64_t device_l2_bytes();
+// feed_R (fused step only, else null): the GEMM's A rows are the operand the
+// vocabulary pass wrote at the start of `ws` (see launch_vocab_pass_feed),
+// which the materialisation pass completes for rows where feed_R is NaN.
 cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
-                            void *ws, const SelfcondPlan &plan, cudaStream_t s);
+                            void *ws, const SelfcondPlan &plan, cudaStream_t s,
+                            const float *feed_R = nullptr);
 
 // Copies the self-cond GEMM's first wait-timeout record to host memory
 // (synchronous; diagnostics only).

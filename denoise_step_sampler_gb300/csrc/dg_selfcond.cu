@@ -286,6 +286,10 @@ struct GemmArgs {
   uint32_t *status;
   float cap_k, cap_c;  // logit softcap: 2 log2(e) / c and c (capped kernels only)
   float scale;         // factor on the output (the embedding scale; 1 = none)
+  // fused step (else null): per row, the reference R of the operand the
+  // vocabulary pass wrote (the A rows hold 2^(z c - R)), or NaN for rows the
+  // materialisation pass wrote as p itself
+  const float *feed_R;
 };
 
 __device__ __forceinline__ bool row_feeds(const GemmArgs &a, int64_t q, float &c, float &l2) {
@@ -688,6 +692,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     have = __all_sync(0xFFFFFFFFu, have);
     tc_fence_after();
     const bool ok = have && sh->row_ok[r] != 0;
+    // fused step: rows the vocabulary pass wrote hold 2^(z c - R); times
+    // 2^(R - l2) they are p
+    float g = 1.f;
+    if (ok && a.feed_R) {
+      float c_, l2_;
+      row_feeds(a, q, c_, l2_);
+      const float R = a.feed_R[q];
+      if (isfinite(R)) g = exp2f(R - l2_);
+    }
     for (int cb = cbase; cb < cbase + BN / 2; cb += 32) {
       const int col0 = n0 + cb;
       if (col0 >= a.d) break;  // warp-uniform
@@ -700,9 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      } else if (a.splits == 1) {  // split partials are scaled by the reduction
+      } else {  // split partials get the embedding scale in the reduction
+        const float f = a.splits == 1 ? a.scale * g : g;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] *= a.scale;
+        for (int j = 0; j < 32; ++j) v[j] *= f;
       }
       if (q < a.rows && a.splits > 1 && run) {
         // (rows that do not feed get zeros from the reduction)
@@ -767,6 +781,7 @@ __global__ void __launch_bounds__(256) selfcond_pmat_kernel(GemmArgs a, uint4 *p
   const int64_t q = blockIdx.x;
   float c = 0.f, l2 = 0.f;
   if (!row_feeds(a, q, c, l2)) return;
+  if (a.feed_R && isfinite(a.feed_R[q])) return;  // the vocabulary pass wrote this row
   constexpr size_t esz = DT == DG_BF16 ? 2 : 4;
   const char *rowp = reinterpret_cast<const char *>(a.logits) + (size_t)q * (size_t)a.ld * esz;
   uint4 *prow = p + (size_t)q * (size_t)(p_ld / 8);
@@ -917,7 +932,8 @@ cudaError_t launch_gemm(const CUtensorMap &map_e, const CUtensorMap &map_z,
 
 cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_state &st,
                             const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
-                            void *ws, const SelfcondPlan &plan, cudaStream_t s) {
+                            void *ws, const SelfcondPlan &plan, cudaStream_t s,
+                            const float *feed_R) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const int64_t rows = (int64_t)p.batch * p.canvas_len;
@@ -1009,6 +1025,7 @@ cudaError_t launch_selfcond(const dg_params &p, const void *logits, const dg_sta
   a.cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
   a.cap_c = cap ? p.softcap : 0.f;
   a.scale = p.embed_scale > 0.f ? p.embed_scale : 1.0f;
+  a.feed_R = feed_R;
 
   cudaError_t e;
   if (pre) {

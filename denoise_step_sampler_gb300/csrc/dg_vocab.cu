@@ -635,7 +635,7 @@ __device__ __forceinline__ int32_t segment_inner_draw(const void *row, int32_t V
 // registers).  SEG: the candidate follows the segmented rule (no Gumbel
 // screen, queue or shared bound; one draw per segment of 32 indices, then the
 // inner draw).
-template <int DT, bool CAP, bool SEG>
+template <int DT, bool CAP, bool SEG, bool FEED>
 // bf16 kernels run 3 CTAs of 8 warps per SM (the ring and the queues fill
 // shared memory), at most 80 registers per thread; fp32 ones 4 CTAs at 64.
 __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
@@ -644,7 +644,9 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
                       float cap_k, float cap_c,
                       const uint8_t *__restrict__ phase, const uint64_t *__restrict__ request_id,
                       const float *__restrict__ temperature, const uint64_t *__restrict__ rng_step,
-                      Partial *__restrict__ part, uint32_t *__restrict__ status) {
+                      Partial *__restrict__ part, uint32_t *__restrict__ status,
+                      uint4 *__restrict__ feed_p, int64_t feed_ld8,
+                      const float *__restrict__ m_prev) {
   __shared__ int32_t s_bound[kWarps];  // best score per position handled by this CTA
   __shared__ QEntry s_queue[kWarps][SEG ? 1 : kQueue];
   extern __shared__ uint4 s_ring[];
@@ -705,6 +707,8 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
   Lane L;
   lane_init(L);
   uint32_t flags = 0;
+  bool feed_ok = false;  // FEED: this lane wrote every operand slot of its share
+  float feed_R = 0.f;
 
   // ---- fast path over full groups.  Lanes walk the chunk in warp-uniform
   // rounds (every lane runs the same number of iterations, partial rounds are
@@ -761,6 +765,17 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(
         s_ring + (size_t)(threadIdx.x >> 5) * (kStages * 128) + lane);
     const uint4 *nxt = vrow + lane;
+    // FEED: this lane's first 16-byte slot of the feed operand row, and
+    // the row's reference R; feed_f = 2^(m2 - R) turns a sum term 2^(z c - m2)
+    // into the operand's 2^(z c - R)
+    uint4 *frow = nullptr;
+    if constexpr (FEED) {
+      const float mp = m_prev[pos];
+      feed_ok = isfinite(mp);
+      feed_R = feed_ok ? ceilf(mp * kLog2e) + kFeedMargin : 0.f;
+      frow = feed_p + (size_t)pos * (size_t)feed_ld8 + g0 + lane;
+    }
+    float feed_f = 0.f;
 #pragma unroll
     for (int r = 0; r < kStages - 1; ++r) {
       if (r < rounds) {
@@ -801,9 +816,16 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
       const float xr = rmax * c;
       if (xr > L.m2 + kLazyRef) rescale(L, ceilf(xr));  // the first finite round sets it
       const float2 mm = make_float2(-L.m2, -L.m2);
+      if constexpr (FEED) {
+        // terms above 2^(R + 96) could overflow the operand: the position
+        // will take the fallback (its new maximum fails the span test)
+        if (L.m2 - feed_R > kFeedSpan) feed_ok = false;
+        feed_f = pow2_int(fmaxf(L.m2 - feed_R, -127.f));
+      }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t pw[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           float zl = __uint_as_float(w[k] << 16), zh = __uint_as_float(w[k] & 0xFFFF0000u);
@@ -813,6 +835,11 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
           }
           const float2 a = __ffma2_rn(make_float2(zl, zh), cc, mm);
           const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+          if constexpr (FEED) {
+            const float2 pf = __fmul2_rn(e, make_float2(feed_f, feed_f));
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(pf.x, pf.y);
+            pw[k] = *reinterpret_cast<const uint32_t *>(&pb);
+          }
           if (SEG && u == 0 && k < 2) {
             // the segmented rule's round sums start from the round's first
             // pairs instead of from zeros (the same values: 0 + e = e)
@@ -831,6 +858,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
             L.T0 = __ffma2_rn(a, e, L.T0);
           }
         }
+        if constexpr (FEED) frow[(size_t)rd * 128 + u * 32] = make_uint4(pw[0], pw[1], pw[2], pw[3]);
       }
       if constexpr (SEG) {
         // the round is lane's whole segment of superblock (v0 / 1024 + rd):
@@ -864,6 +892,10 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
       }
       if ((rd & 15) == 15) fold_block(L); else fold_round(L);
       share_bound(slot, wb, lane);
+    }
+    if constexpr (FEED) {
+      // columns outside whole rounds get no operand: the position falls back
+      if (rounds * 128 != n_full || tail_n > 0) feed_ok = false;
     }
     // the segmented rule's round sums hold the last round's values (already
     // folded); the paths after the ring add to them from zero
@@ -974,6 +1006,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
   const bool bad = !(isfinite(s) && isfinite(t));
   if (__any_sync(0xFFFFFFFFu, bad)) {
     // ---- careful path: redo the whole chunk
+    feed_ok = false;
     lane_init(L);
     for (int q = lane; q < n_full; q += 32) {
       float z[8];
@@ -998,6 +1031,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
     cand = segment_inner_draw<DT, CAP>(row, V, cand, c, K, cap_k, cap_c, lane);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, off);
+  if (FEED && __all_sync(0xFFFFFFFFu, feed_ok)) flags |= kPartFeed;
   if (lane == 0) {
     Partial P;
     P.zmax = zmax;
@@ -1007,7 +1041,7 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
     P.b2 = b2;
     P.cand = cand;
     P.flags = flags;
-    P.pad = 0;
+    P.pad = FEED ? __float_as_uint(feed_R) : 0u;
     *out = P;
   }
 }
@@ -1026,16 +1060,19 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, false>,
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, false, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true>,
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, false>,
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, false, false>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
-      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, true>,
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, true, true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+      if (e != cudaSuccess) return e;
+      e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true, true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
       if (e != cudaSuccess) return e;
       if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
@@ -1045,10 +1082,11 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   const float cap_k = cap ? 2.0f * kLog2e / p.softcap : 0.f;
   const float cap_c = cap ? p.softcap : 0.f;
 #define DG_VOCAB_LAUNCH(DT, CAP, SEG)                                                         \
-  vocab_pass_kernel<DT, CAP, SEG><<<(unsigned)blocks, kWarps * 32,                           \
-                                    DT == DG_BF16 ? kRingBytes : 0, s>>>(                     \
+  vocab_pass_kernel<DT, CAP, SEG, false><<<(unsigned)blocks, kWarps * 32,                    \
+                                           DT == DG_BF16 ? kRingBytes : 0, s>>>(              \
       logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c, \
-      st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status)
+      st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status, nullptr, 0, \
+      nullptr)
   const bool seg = p.sample_rule == DG_SAMPLE_SEGMENTED;
   if (p.logits_dtype == DG_BF16) {
     if (cap) {
@@ -1068,6 +1106,32 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
     }
   }
 #undef DG_VOCAB_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vocab_pass_feed(const dg_params &p, const void *logits, const dg_state &st,
+                                   Partial *part, int32_t chunk, int32_t n_chunks,
+                                   uint4 *feed_p, int64_t feed_ld8, cudaStream_t s) {
+  // the caller has checked: bf16 rows on 16-byte boundaries, segmented rule,
+  // no softcap; the attribute was set by launch_vocab_pass's first call or here
+  const int64_t n_pos = (int64_t)p.batch * p.canvas_len;
+  const int64_t warps = n_pos * n_chunks;
+  const int64_t blocks = (warps + kWarps - 1) / kWarps;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  static std::atomic<bool> attr_set[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
+  }
+  vocab_pass_kernel<DG_BF16, false, true, true><<<(unsigned)blocks, kWarps * 32, kRingBytes, s>>>(
+      logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, 0.f, 0.f,
+      st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status, feed_p,
+      feed_ld8, st.m);
   return cudaGetLastError();
 }
 

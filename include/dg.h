@@ -224,6 +224,29 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
                       const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
                       void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* The sampler step and the self-conditioning feed in one call: the same
+ * results as dg_denoise_step followed by dg_selfcond_embed on the same
+ * stream (outputs equal; the feed within the same tolerance), with the
+ * logits read once for both where the inputs allow.  For bf16 logits whose
+ * rows start on 16-byte boundaries, under DG_SAMPLE_SEGMENTED and without a
+ * softcap, the vocabulary pass also writes the feed's operand
+ * 2^(z c - R) (bf16, c = log2(e)/T) into the workspace as it streams the
+ * logits, with R = ceil(m' log2 e) + 32 from each position's previous
+ * maximum m' (st->m before the call); positions whose new maximum z_max
+ * leaves |z_max c - R| > 96 (the first step of a request, large jumps), or
+ * whose logits are not finite, get p written by a separate pass instead.
+ * The GEMM then reads the operand without rebuilding it, and each output row
+ * is scaled by 2^(R - log2 sum 2^(z c)).  Other inputs run the two calls in
+ * turn.  Arguments as for the two calls; `ws`: at least
+ * dg_workspace_bytes_feed(p, d) bytes (about B*C*V*2 bytes more than
+ * dg_workspace_bytes(p, d) below 1,024 positions).  Three to five kernel
+ * launches.  The pages describe the two steps apart; the fusion is this
+ * library's. */
+size_t dg_workspace_bytes_feed(const dg_params *p, int32_t d);
+int dg_denoise_step_feed(const dg_params *p, const void *logits, const dg_state *st,
+                         const void *E, int32_t d, int64_t ld_E, void *out, int32_t out_dtype,
+                         void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Stand-alone commit (the commit case) of the rows with row_mask[r] != 0:
  * emitted = argmax_prev (the clean argmax canvas, vLLM blog "Entropy-bounded
  * denoising"), num_sampled = C, num_rejected = 0, a fresh random canvas,
