@@ -487,10 +487,9 @@ def _feed_launches(p, d):
     ld = p.logits_ld or p.vocab
     rows = p.batch * p.canvas_len
     unaligned = (ld * 2) % 16 != 0
-    if p.logits_dtype != dg.DG_BF16 or p.softcap > 0 or unaligned or \
-            p.sample_rule != dg.DG_SAMPLE_SEGMENTED:
+    if p.logits_dtype != dg.DG_BF16 or unaligned or p.sample_rule != dg.DG_SAMPLE_SEGMENTED:
         return _selfcond_launches(p, d) - 1
-    two_call_materialises = rows >= 1024
+    two_call_materialises = rows >= 1024 or p.softcap > 0
     has_reduce = _selfcond_launches(p, d) - 1 - (1 if two_call_materialises else 0)
     return 1 + has_reduce
 

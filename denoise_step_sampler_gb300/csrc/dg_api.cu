@@ -228,12 +228,11 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
 
 namespace {
 // The fused step writes the feed's operand from the vocabulary pass for bf16
-// rows on 16-byte boundaries under the segmented rule without a softcap;
+// rows on 16-byte boundaries under the segmented rule (softcapped or not);
 // other inputs run the two calls in turn.
 bool feed_fusable(const dg_params &p, const void *logits) {
-  return p.logits_dtype == DG_BF16 && !(p.softcap > 0.f) &&
-         p.sample_rule == DG_SAMPLE_SEGMENTED && (p.logits_ld * 2) % 16 == 0 &&
-         aligned(logits, 16);
+  return p.logits_dtype == DG_BF16 && p.sample_rule == DG_SAMPLE_SEGMENTED &&
+         (p.logits_ld * 2) % 16 == 0 && aligned(logits, 16);
 }
 // Workspace of the fused step: [vocabulary-pass records][per-position R]
 // [the operand rows (the self-cond plan's p) | split-K partial sums].

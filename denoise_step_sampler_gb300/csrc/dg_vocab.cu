@@ -1109,11 +1109,11 @@ cudaError_t launch_vocab_pass(const dg_params &p, const void *logits, const dg_s
   return cudaGetLastError();
 }
 
-cudaError_t launch_vocab_pass_feed(const dg_params &p, const void *logits, const dg_state &st,
-                                   Partial *part, int32_t chunk, int32_t n_chunks,
-                                   uint4 *feed_p, int64_t feed_ld8, cudaStream_t s) {
-  // the caller has checked: bf16 rows on 16-byte boundaries, segmented rule,
-  // no softcap; the attribute was set by launch_vocab_pass's first call or here
+namespace {
+template <bool CAP>
+cudaError_t vocab_pass_feed_launch(const dg_params &p, const void *logits, const dg_state &st,
+                                   Partial *part, int32_t chunk, int32_t n_chunks, uint4 *feed_p,
+                                   int64_t feed_ld8, cudaStream_t s) {
   const int64_t n_pos = (int64_t)p.batch * p.canvas_len;
   const int64_t warps = n_pos * n_chunks;
   const int64_t blocks = (warps + kWarps - 1) / kWarps;
@@ -1123,16 +1123,29 @@ cudaError_t launch_vocab_pass_feed(const dg_params &p, const void *logits, const
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev].load(std::memory_order_relaxed)) {
-    e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, false, true, true>,
+    e = cudaFuncSetAttribute(vocab_pass_kernel<DG_BF16, CAP, true, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kRingBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev].store(true, std::memory_order_relaxed);
   }
-  vocab_pass_kernel<DG_BF16, false, true, true><<<(unsigned)blocks, kWarps * 32, kRingBytes, s>>>(
-      logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, 0.f, 0.f,
+  const float cap_k = CAP ? 2.0f * kLog2e / p.softcap : 0.f;
+  const float cap_c = CAP ? p.softcap : 0.f;
+  vocab_pass_kernel<DG_BF16, CAP, true, true><<<(unsigned)blocks, kWarps * 32, kRingBytes, s>>>(
+      logits, p.logits_ld, p.vocab, p.canvas_len, n_pos, chunk, n_chunks, p.seed, cap_k, cap_c,
       st.phase, st.request_id, st.temperature, st.rng_step, part, st.device_status, feed_p,
       feed_ld8, st.m);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_vocab_pass_feed(const dg_params &p, const void *logits, const dg_state &st,
+                                   Partial *part, int32_t chunk, int32_t n_chunks,
+                                   uint4 *feed_p, int64_t feed_ld8, cudaStream_t s) {
+  // the caller has checked: bf16 rows on 16-byte boundaries, segmented rule
+  return p.softcap > 0.f
+             ? vocab_pass_feed_launch<true>(p, logits, st, part, chunk, n_chunks, feed_p, feed_ld8, s)
+             : vocab_pass_feed_launch<false>(p, logits, st, part, chunk, n_chunks, feed_p, feed_ld8,
+                                             s);
 }
 
 }  // namespace dg

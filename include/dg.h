@@ -228,8 +228,9 @@ int dg_selfcond_embed(const dg_params *p, const void *logits, const dg_state *st
  * results as dg_denoise_step followed by dg_selfcond_embed on the same
  * stream (outputs equal; the feed within the same tolerance), with the
  * logits read once for both where the inputs allow.  For bf16 logits whose
- * rows start on 16-byte boundaries, under DG_SAMPLE_SEGMENTED and without a
- * softcap, the vocabulary pass also writes the feed's operand
+ * rows start on 16-byte boundaries, under DG_SAMPLE_SEGMENTED (with or
+ * without a softcap; with one, z below is the capped logit), the vocabulary
+ * pass also writes the feed's operand
  * 2^(z c - R) (bf16, c = log2(e)/T) into the workspace as it streams the
  * logits, with R = ceil(m' log2 e) + 32 from each position's previous
  * maximum m' (st->m before the call); positions whose new maximum z_max

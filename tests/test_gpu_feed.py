@@ -6,8 +6,9 @@ sampler output bit for bit (the vocabulary pass's arithmetic is the same),
 and the feed against the fp64 oracle within the feed tolerance.  Covered:
 first and second steps; positions whose previous maximum is far from the new
 one (the operand would leave bf16's range: p is written by a separate pass
-instead); rows that do not feed; and inputs the fusion does not take
-(unaligned rows, the softcap, the grouped rule), which run the two calls."""
+instead); rows that do not feed; the softcap with the embedding scale; and
+inputs the fusion does not take (unaligned rows, the grouped rule), which run
+the two calls."""
 
 import numpy as np
 import pytest
@@ -17,6 +18,7 @@ import denoise_step_sampler_gb300 as dg
 from denoise_step_sampler_gb300 import synthetic as syn
 
 from _gpu_common import make_state, oracle_selfcond_rows, selfcond_check
+from oracle import selfcond as osc
 
 pytestmark = pytest.mark.gpu
 
@@ -40,13 +42,17 @@ def _clone(st: dg.State) -> dg.State:
     return c
 
 
-def _check_feed(got, logits2d, T, Eh, rows, C):
+def _check_feed(got, logits2d, T, Eh, rows, C, cap=0.0, scale=0.0):
     # rows grouped by canvas (one temperature each), one fp64 product per group
     rows = np.asarray(rows)
     for r in np.unique(rows // C):
         sel = rows[rows // C == r]
         z = logits2d[torch.as_tensor(sel, device=logits2d.device)].float().cpu().numpy()
-        ref = oracle_selfcond_rows(z.astype(np.float64), float(np.float32(T[r])), Eh)
+        if cap > 0 or scale > 0:
+            ref = osc.selfcond_rows(z.astype(np.float64), float(np.float32(T[r])), Eh,
+                                    cap=float(np.float32(cap)), scale=float(np.float32(scale)))
+        else:
+            ref = oracle_selfcond_rows(z.astype(np.float64), float(np.float32(T[r])), Eh)
         selfcond_check(got[sel], ref)
 
 
@@ -80,7 +86,7 @@ def _steps(p, phases, logits, E, temps, n_steps=2, m_init=None, out_dtype=torch.
             rows = rows[np.linspace(0, len(rows) - 1, sample_rows).astype(int)]
         ldv = logits.numel() // n
         _check_feed(gb, logits.view(n, ldv)[:, :p.vocab], temps_arr(temps, p.batch), Eh, rows,
-                    p.canvas_len)
+                    p.canvas_len, cap=p.softcap, scale=p.embed_scale)
     return st_b
 
 
@@ -128,14 +134,12 @@ def test_feed_rows_that_do_not_feed_and_bf16_output():
     _steps(p, phases, logits, E, [0.9, 1.0, 1.0, 1.1], n_steps=3, out_dtype=torch.bfloat16)
 
 
-@pytest.mark.parametrize("kind", ["unaligned", "softcap", "grouped"])
+@pytest.mark.parametrize("kind", ["unaligned", "grouped"])
 def test_feed_inputs_that_take_the_two_calls(kind):
     B, C, V, d = 2, 128, 5000, 128
     kw = dict(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=9,
               entropy_budget=40.0, conf_threshold=-1.0, stable_k=3, step_cap=1000,
               sample_rule=dg.DG_SAMPLE_SEGMENTED)
-    if kind == "softcap":
-        kw["softcap"] = 30.0
     if kind == "grouped":
         kw["sample_rule"] = dg.DG_SAMPLE_GROUPED
     p = dg.Params(**kw)
@@ -161,6 +165,33 @@ def test_feed_inputs_that_take_the_two_calls(kind):
     sa, sb = st_a.snapshot(), st_b.snapshot()
     for k in FIELDS:
         assert np.array_equal(np.asarray(sa[k]), np.asarray(sb[k]), equal_nan=True), k
+
+
+@pytest.mark.parametrize("B,C,V,d,cap,scale",
+                         [(2, 256, 8192, 256, 30.0, 16.0), (3, 128, 4096, 128, 15.0, 0.0),
+                          (2, 64, 2048, 64, 50.0, 8.0)],
+                         ids=["B2V8192c30", "B3V4096c15", "B2V2048c50"])
+def test_feed_softcap_matches_the_two_calls_and_the_oracle(B, C, V, d, cap, scale):
+    # the vocabulary pass writes 2^(c_cap tanh(z / c_cap) c - R); the first
+    # step has no previous maximum (every row takes the separate pass), the
+    # later ones keep the operand
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=77,
+                  entropy_budget=40.0, conf_threshold=-1.0, stable_k=3, step_cap=1000,
+                  sample_rule=dg.DG_SAMPLE_SEGMENTED, softcap=cap, embed_scale=scale)
+    temps = list(np.linspace(0.6, 1.3, B))
+    logits = syn.boosted_logits(B * C, V, seed=V + 5, device="cuda", boost_hi=24.0).reshape(-1)
+    E = syn.embedding(V, d, seed=d + 1, device="cuda")
+    _steps(p, [dg.DG_PHASE_DENOISE] * B, logits, E, temps, n_steps=3, sample_rows=48)
+
+
+def test_feed_at_eight_canvases_full_vocabulary_softcap():
+    B, C, V, d = 8, 256, 262144, 2816
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=0xD1FF000C,
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  sample_rule=dg.DG_SAMPLE_SEGMENTED, softcap=30.0, embed_scale=53.066)
+    logits = syn.boosted_logits(B * C, V, seed=15, device="cuda").reshape(-1)
+    E = syn.embedding(V, d, seed=16, device="cuda")
+    _steps(p, [dg.DG_PHASE_DENOISE] * B, logits, E, [0.8] * B, n_steps=2, sample_rows=16)
 
 
 def test_feed_at_eight_canvases_full_vocabulary():
