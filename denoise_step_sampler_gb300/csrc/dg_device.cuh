@@ -103,13 +103,30 @@ __device__ __forceinline__ float pow2_int(float d) {
   return e < -126 ? 0.f : __int_as_float((127 + e) << 23);
 }
 
+// 1/x by the hardware's approximate reciprocal (PTX rcp.approx.ftz.f32:
+// at most 1 ulp from 1/x; +inf gives +0).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Logit softcap c tanh(z / c), from tanh x = 1 - 2 / (e^(2x) + 1):
-// c - 2c / (2^(z k) + 1) with k = 2 log2(e) / c.  +-inf map to +-c and NaN
-// stays NaN.  The absolute error is a few 1e-7 c (ex2.approx and the rounded
-// reciprocal near e = 1, where the slope is largest).
+// c - 2c / (2^(z k) + 1) with k = 2 log2(e) / c.  +inf maps to c, -inf to
+// c - 2c rcp(1) and NaN stays NaN.  The absolute error is a few 1e-7 c: the
+// relative errors of ex2.approx and of the reciprocal (each within an ulp or
+// two), times 2c / (e + 1) <= 2c.  Two MUFU operations per logit.
 __device__ __forceinline__ float softcap_f(float z, float k, float c) {
   const float e = ex2_approx(__fmul_rn(z, k));
-  return fmaf(-2.0f * c, __frcp_rn(__fadd_rn(e, 1.0f)), c);
+  return fmaf(-2.0f * c, rcp_approx(__fadd_rn(e, 1.0f)), c);
+}
+// The same on a pair with f32x2 arithmetic, bit for bit (each lane of a
+// packed multiply, add or fma rounds as the scalar one does).
+__device__ __forceinline__ float2 softcap2_f(float2 z, float k, float c) {
+  const float2 t = __fmul2_rn(z, make_float2(k, k));
+  const float2 x = __fadd2_rn(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+  return __ffma2_rn(make_float2(rcp_approx(x.x), rcp_approx(x.y)),
+                    make_float2(-2.0f * c, -2.0f * c), make_float2(c, c));
 }
 
 // Packed pairs of fp32 (Blackwell f32x2 arithmetic).

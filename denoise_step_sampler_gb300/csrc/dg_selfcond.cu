@@ -385,9 +385,12 @@ __device__ __forceinline__ uint4 p_from_bf16_cap(const uint32_t (&w)[4], float c
                                                  int valid, float cap_k, float cap_c) {
   float p[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float z = __uint_as_float((j & 1) ? (w[j >> 1] & 0xFFFF0000u) : (w[j >> 1] << 16));
-    p[j] = (j < valid) ? ex2_approx(fmaf(softcap_f(z, cap_k, cap_c), c, -l2)) : 0.f;
+  for (int j = 0; j < 8; j += 2) {
+    const float2 zc = softcap2_f(make_float2(__uint_as_float(w[j >> 1] << 16),
+                                             __uint_as_float(w[j >> 1] & 0xFFFF0000u)),
+                                 cap_k, cap_c);
+    p[j] = (j < valid) ? ex2_approx(fmaf(zc.x, c, -l2)) : 0.f;
+    p[j + 1] = (j + 1 < valid) ? ex2_approx(fmaf(zc.y, c, -l2)) : 0.f;
   }
   return make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
                     pack_bf16x2(p[6], p[7]));

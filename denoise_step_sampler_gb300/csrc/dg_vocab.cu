@@ -830,8 +830,9 @@ __global__ void __launch_bounds__(kWarps * 32, DT == DG_BF16 ? 3 : 4)
         for (int k = 0; k < 4; ++k) {
           float zl = __uint_as_float(w[k] << 16), zh = __uint_as_float(w[k] & 0xFFFF0000u);
           if (CAP) {
-            zl = softcap_f(zl, cap_k, cap_c);
-            zh = softcap_f(zh, cap_k, cap_c);
+            const float2 zc = softcap2_f(make_float2(zl, zh), cap_k, cap_c);
+            zl = zc.x;
+            zh = zc.y;
           }
           const float2 a = __ffma2_rn(make_float2(zl, zh), cc, mm);
           const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
