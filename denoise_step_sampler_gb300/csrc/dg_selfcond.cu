@@ -874,17 +874,27 @@ SelfcondPlan selfcond_plan(int64_t rows, int32_t V, int32_t d, int32_t n_sms, in
   pl.k_blocks = (V + BK - 1) / BK;
   const int64_t tiles = (int64_t)pl.m_tiles * pl.n_tiles;
   const int64_t sms = n_sms > 0 ? n_sms : 1;
-  // Choose the split count whose CTA count fills the SMs best (waves of one
-  // CTA per SM), keeping at least 16 k-blocks per split.
+  // Choose the split count of least estimated time, in units of one CTA's
+  // k-block (waves of one CTA per SM, at least 16 k-blocks per split):
+  //   waves * (k-blocks per split + kCtaFixedKb) + the reduction's traffic.
+  // A CTA's fixed cost (barriers and TMEM set up, the rings filled, the
+  // accumulator drained) came to ~25 us, about 38 k-blocks of tensor work,
+  // in measured sweeps on a GB300; the reduction moves 8 bytes per partial
+  // sum, ~4.4 MB per k-block's time at the copy rate.  At one canvas this
+  // picks 13 splits (one wave) where filling whole waves picked 55: 22 %
+  // less time for the step.
+  constexpr double kCtaFixedKb = 38.0;
+  constexpr double kReduceBytesPerKb = 4.4e6;
   int best = 1;
-  double best_eff = 0.0;
+  double best_cost = 0.0;
   for (int sp = 1; sp <= 64; ++sp) {
     if (sp > 1 && pl.k_blocks / sp < 16) break;
-    const int64_t ctas = tiles * sp;
-    const int64_t waves = (ctas + sms - 1) / sms;
-    const double eff = (double)ctas / (double)(waves * sms);
-    if (eff > best_eff + 0.05) {
-      best_eff = eff;
+    const int64_t waves = (tiles * sp + sms - 1) / sms;
+    const int64_t kbps = (pl.k_blocks + sp - 1) / sp;
+    const double red = sp > 1 ? 8.0 * (double)sp * (double)rows * (double)d / kReduceBytesPerKb : 0.0;
+    const double cost = (double)waves * ((double)kbps + kCtaFixedKb) + red;
+    if (sp == 1 || cost < best_cost) {
+      best_cost = cost;
       best = sp;
     }
   }

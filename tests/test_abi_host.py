@@ -148,9 +148,11 @@ def test_workspace_follows_the_split_plan(L):
     # the self-conditioning workspace is the materialised p (bf16 rows of V
     # rounded up to 8, from 1,024 positions on, and for softcapped feeds)
     # followed by [splits][B*C][d] fp32 partial sums; on a 152-SM part with
-    # 129 MiB of L2 (the values used when no device can be queried):
-    #  - 8 and 64 canvases take the split count that fills the SMs in whole
-    #    waves (5 and 3);
+    # 129 MiB of L2 (the values used when no device can be queried), the split
+    # count of least cost waves * (k-blocks per split + 38) + reduction bytes /
+    # 4.4 MB:
+    #  - 1 and 2 canvases: 13 and 6 splits, one wave of 143 and 132 CTAs;
+    #  - 8 and 64 canvases: 5 and 3 (three and fourteen waves);
     #  - 128 canvases (more than 64 row tiles of 256) split further, until one
     #    split's slice of E fits in L2: 11 splits (10 would leave 148 MB)
     V, d = 262144, 2816
@@ -159,10 +161,11 @@ def test_workspace_follows_the_split_plan(L):
         p = dg.Params(batch=B, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16)
         assert dg.dg_workspace_bytes(p, d) == p_bytes(B) + splits * B * 256 * d * 4, B
     assert V * d * 2 // 10 > 135528448 >= V * d * 2 // 11
-    # two canvases rebuild p inside the GEMM: partial sums only, 48 splits
-    # (22 tiles x 48 = 1,056 CTAs, 99 % of 7 waves)
+    # one and two canvases rebuild p inside the GEMM: partial sums only
+    one = dg.Params(batch=1, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16)
+    assert dg.dg_workspace_bytes(one, d) == 13 * 256 * d * 4
     two = dg.Params(batch=2, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16)
     ws2 = dg.dg_workspace_bytes(two, d)
-    assert ws2 == 48 * 2 * 256 * d * 4
+    assert ws2 == 6 * 2 * 256 * d * 4
     capped = dg.Params(batch=2, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16, softcap=30.0)
     assert dg.dg_workspace_bytes(capped, d) == p_bytes(2) + ws2
