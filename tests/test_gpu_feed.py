@@ -194,6 +194,18 @@ def test_feed_at_eight_canvases_full_vocabulary_softcap():
     _steps(p, [dg.DG_PHASE_DENOISE] * B, logits, E, [0.8] * B, n_steps=2, sample_rows=16)
 
 
+def test_feed_at_one_canvas_full_vocabulary():
+    # one wave of 143 GEMM CTAs (13 vocabulary splits), the operand from the
+    # vocabulary pass after the first step
+    B, C, V, d = 1, 256, 262144, 2816
+    p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=0xD1FF000D,
+                  entropy_budget=96.0, conf_threshold=0.3, stable_k=3, step_cap=32,
+                  sample_rule=dg.DG_SAMPLE_SEGMENTED)
+    logits = syn.boosted_logits(B * C, V, seed=17, device="cuda").reshape(-1)
+    E = syn.embedding(V, d, seed=18, device="cuda")
+    _steps(p, [dg.DG_PHASE_DENOISE] * B, logits, E, [0.8] * B, n_steps=2, sample_rows=16)
+
+
 def test_feed_at_eight_canvases_full_vocabulary():
     B, C, V, d = 8, 256, 262144, 2816
     p = dg.Params(batch=B, canvas_len=C, vocab=V, logits_dtype=dg.DG_BF16, seed=0xD1FF000A,

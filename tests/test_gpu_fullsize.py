@@ -9,7 +9,7 @@ times:
   self-conditioning rows from every 256-row tile of the GEMM;
 * the same with the logit softcap (c = 30) and the sqrt(d) embedding scale,
   at 8 and at 128 canvases;
-* 16, 32 and 64 canvases (the sweep sizes) and 128 canvases x 256 (17 GB of
+* 1, 2, 4, 16, 32 and 64 canvases (the sweep sizes) and 128 canvases x 256 (17 GB of
   logits, both sampling rules): one full canvas, 64 random positions, two
   self-conditioning rows from every 256-row tile of the GEMM;
 * the mixed-phase loop (32 requests: 8 prefill, 20 denoise, 4 commit) at
@@ -146,12 +146,15 @@ def test_eight_canvases_V262144_bf16_sampled(rule):
               sample_rule=rule)
 
 
-@pytest.mark.parametrize("B,seed", [(16, 0xD1FF0007), (32, 0xD1FF0006), (64, 0xD1FF0008)],
-                         ids=["16", "32", "64"])
+@pytest.mark.parametrize("B,seed", [(1, 0xD1FF0011), (2, 0xD1FF0012), (4, 0xD1FF0013),
+                                    (16, 0xD1FF0007), (32, 0xD1FF0006), (64, 0xD1FF0008)],
+                         ids=["1", "2", "4", "16", "32", "64"])
 def test_sweep_canvases_V262144_bf16_sampled(B, seed):
-    # the sweep sizes: other split plans of the GEMM (on 152 SMs: 6 splits at
-    # 16 canvases, 3 from 32 on) and 4 or 2 vocabulary chunks per position
-    _one_step(B, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, seed, 64, 2,
+    # the sweep sizes: other split plans of the GEMM (on 152 SMs: 13 splits
+    # at one canvas and 6 at two, one wave each, with p rebuilt in the GEMM;
+    # 10 at four and 6 at 16 canvases, 3 from 32 on, on a materialised p) and
+    # 8, 4 or 2 vocabulary chunks per position
+    _one_step(B, 256, 262144, dg.DG_BF16, 0.8, 128.0, 2816, 16.0, seed, 64, 8 if B <= 2 else 2,
               sample_rule=dg.DG_SAMPLE_SEGMENTED)
 
 
