@@ -166,11 +166,12 @@ typedef struct {
  * dg_selfcond_embed with embedding width d (one buffer serves both, as the
  * calls are ordered on one stream).  Returns 0 if `p` is invalid.  Depends on
  * the sizes in `p`, on d and on the SM count and L2 size of the current
- * device (the self-conditioning GEMM splits the vocabulary to fill the SMs in
- * whole waves and, for more than 64 row tiles of 256 positions, until one
- * split's slice of E fits in L2); query it with the device current that the
- * calls will run on.  With d > 0 it
- * includes the feed's materialised probabilities, B*C rows of V rounded up to
+ * device (the self-conditioning GEMM splits the vocabulary by a cost model of
+ * its waves of CTAs and of the split-K reduction and, for more than 64 row
+ * tiles of 256 positions, further until one split's slice of E fits in L2;
+ * the partial sums take splits*B*C*d*4 bytes); query it with the device
+ * current that the calls will run on.  With d > 0 it includes the feed's
+ * materialised probabilities, B*C rows of V rounded up to
  * 8 bf16 (about B*C*V*2 bytes: 1.07 GB for 8 x 256 positions at V = 262,144,
  * 17.2 GB for 128 x 256), when B*C >= 1024, when p->softcap > 0, or when the
  * logits are fp32 or bf16 rows whose stride (logits_ld * 2 bytes) is not a
