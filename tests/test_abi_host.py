@@ -169,3 +169,45 @@ def test_workspace_follows_the_split_plan(L):
     assert ws2 == 6 * 2 * 256 * d * 4
     capped = dg.Params(batch=2, canvas_len=256, vocab=V, logits_dtype=dg.DG_BF16, softcap=30.0)
     assert dg.dg_workspace_bytes(capped, d) == p_bytes(2) + ws2
+
+
+def test_fused_step_workspace_and_arguments_on_host(L):
+    # dg_workspace_bytes_feed: 0 for invalid params or widths, else at least
+    # the two calls' workspace (the fused call may fall back to them)
+    for B in (1, 8):
+        p = _params(batch=B, logits_dtype=dg.DG_BF16, vocab=4096,
+                    sample_rule=dg.DG_SAMPLE_SEGMENTED)
+        for d in (16, 256):
+            assert dg.dg_workspace_bytes_feed(p, d) >= dg.dg_workspace_bytes(p, d) > 0
+        for d in (0, 8, 24):
+            assert dg.dg_workspace_bytes_feed(p, d) == 0, d
+    assert dg.dg_workspace_bytes_feed(_params(batch=0), 64) == 0
+    assert L.dg_workspace_bytes_feed(None, 64) == 0
+    # dg_denoise_step_feed rejects bad arguments before any device work
+    p = _params(logits_dtype=dg.DG_BF16, vocab=4096, sample_rule=dg.DG_SAMPLE_SEGMENTED).c()
+    st = _fake_state()
+    fake, E, out, ws = (ctypes.c_void_p(a) for a in (0x7000, 0xA000, 0xB000, 0x9000))
+    d = 64
+    need = L.dg_workspace_bytes_feed(ctypes.byref(p), d)
+    ok = [ctypes.byref(p), fake, ctypes.byref(st), E, d, d, out, dg.DG_F32, ws, need, None]
+
+    def call(**kw):
+        args = list(ok)
+        for k, v in kw.items():
+            args[["p", "logits", "st", "E", "d", "ldE", "out", "odt", "ws", "n", "s"].index(k)] = v
+        return L.dg_denoise_step_feed(*args)
+
+    for kw in (dict(p=None), dict(logits=None), dict(st=None), dict(E=None), dict(out=None),
+               dict(d=0), dict(d=24), dict(ldE=32), dict(ldE=68), dict(odt=5),
+               dict(E=ctypes.c_void_p(0xA008)), dict(out=ctypes.c_void_p(0xB004)),
+               dict(logits=ctypes.c_void_p(0x7001))):
+        assert call(**kw) == dg.DG_ERR_INVALID_ARG, kw
+    for field in ("sc_valid", "m", "s"):
+        st2 = _fake_state()
+        setattr(st2, field, None)
+        assert call(st=ctypes.byref(st2)) == dg.DG_ERR_INVALID_ARG, field
+    assert call(n=need - 1) == dg.DG_ERR_WORKSPACE
+    assert call(ws=None) == dg.DG_ERR_WORKSPACE
+    assert call(ws=ctypes.c_void_p(0x9008)) == dg.DG_ERR_WORKSPACE
+    if not torch.cuda.is_available():
+        assert call() in (dg.DG_ERR_CUDA, dg.DG_ERR_UNSUPPORTED)
