@@ -53,15 +53,17 @@ METRIC = "denoise-step positions/s (sampler+self-cond)"
 SEED = 0xD1FF0002
 
 
-def traffic_for(call: str, workload: str):
+def traffic_for(call: str, workload: str, variant: dict):
     """DRAM bytes per call (all of its kernels) from the committed ncu summary,
-    only for the profiled workload and only while every source file of the
-    call is unchanged since the capture (else None)."""
+    only for the profiled workload and variant (the options that select other
+    kernels: softcap on or off, sampling, acceptance and stop rules) and only
+    while every source file of the call is unchanged since the capture (else
+    None)."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             ent = json.load(f)[call]
-        if ent["workload"] != workload:
+        if ent["workload"] != workload or ent["variant"] != variant:
             return None
         for name, want in ent["sources"].items():
             src = os.path.join(ROOT, "denoise_step_sampler_gb300", "csrc", name)
@@ -392,6 +394,8 @@ def run_ours(args, rank, world, dev):
         return None
     e2e_value = world * n_pos * Ke / (ms_e2e / 1e3) if Ke else None
     hbm, bf16_burst, bf16_sust, src = peaks()
+    variant = {"softcap": args.softcap > 0, "sample_rule": args.sample_rule,
+               "accept_rule": args.accept_rule, "stop_rule": args.stop_rule}
     # the GEMM's peak: the sustained (power-capped) figure when the timed
     # region lasts long enough to reach the cap, else the burst one
     long_region = ms >= 1000.0
@@ -426,7 +430,8 @@ def run_ours(args, rank, world, dev):
                                "reduce), timed on the two-call path over the same workload",
                      "achieved": sc_tflops, "peak": bf16, "unit": "TFLOP/s",
                      "frac": sc_tflops / bf16, "frac_of_burst": sc_tflops / bf16_burst,
-                     "traffic": None if args.batch else traffic_for("dg_selfcond_embed", args.workload),
+                     "traffic": None if args.batch else traffic_for("dg_selfcond_embed", args.workload,
+                                                                    variant),
                      "peak_source": "%s bf16 %s (timed region %.2f s)" % (
                          src, "sustained" if long_region else "burst", ms / 1e3),
                      "flops_per_launch": flops,
@@ -436,7 +441,8 @@ def run_ours(args, rank, world, dev):
                                        "two-call path over the same workload",
                              "achieved": sampler_gbs, "peak": hbm, "unit": "GB/s",
                              "frac": sampler_gbs / hbm,
-                             "traffic": None if args.batch else traffic_for("dg_denoise_step", args.workload),
+                             "traffic": None if args.batch else traffic_for("dg_denoise_step",
+                                                                            args.workload, variant),
                              "peak_source": f"{src} copy", "bytes_per_launch": logit_bytes,
                              "ms_per_launch": ms_sampler},
         "clocks": clk,
